@@ -1,0 +1,176 @@
+/*
+ * nvfp4draft.h -- C ABI of the GB300 (sm_103a) NVFP4 weight-only projection
+ * library for a speculative-decoding draft head.
+ *
+ * NVFP4 weight format used throughout:
+ *   packed  uint8 [n, k/2]  two E2M1 codes per byte; element 2j of a row in the
+ *                           low nibble of byte j, element 2j+1 in the high one.
+ *                           (The [N, K/2] layout is the one the prefill setup of
+ *                           "spark_model/layers/qwen3_attention/prefill_weights.rs"
+ *                           feeds its predequant kernel; 0.5 byte per weight as
+ *                           the LM-head size log in "spark_model/layers/mtp_head/new.rs",
+ *                           MtpHead::new, counts it.)
+ *   scales  uint8 [n, k/16] one E4M3 scale per 16-element block along k, row-major.
+ *   global  float           g = absmax(W) / (6 * 448).
+ *   Dequantised weight: w[n][i] = g * e4m3(scales[n][i/16]) * e2m1(code[n][i]).
+ *
+ * Conventions shared by every call:
+ *   - All pointers except those documented as host pointers are DEVICE
+ *     pointers owned by the caller; the library allocates no memory, keeps no
+ *     global state and never synchronises: work is enqueued on ex->stream
+ *     (a cudaStream_t; NULL = legacy default stream) and the call returns.
+ *   - Arguments are checked on the host before anything is enqueued; a
+ *     non-zero status means nothing was launched.  NVFP4_ERR_CUDA means a
+ *     launch failed after validation (the CUDA error is left for the caller's
+ *     cudaGetLastError).
+ *   - ex->dev_status (nullable, device int32) receives conditions detected on
+ *     the device (non-finite input to the quantiser, a bounded wait that gave
+ *     up).  The library only ever writes non-zero codes there; the caller
+ *     clears it.
+ *   - Concurrent calls on different streams need distinct workspaces.
+ *   - No C++ exception crosses this interface.
+ */
+#ifndef NVFP4DRAFT_H
+#define NVFP4DRAFT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes. */
+#define NVFP4_OK 0
+#define NVFP4_ERR_NULL 1       /* a required pointer is NULL                 */
+#define NVFP4_ERR_SHAPE 2      /* a size is out of range or not a multiple   */
+#define NVFP4_ERR_ALIGN 3      /* a pointer or leading dimension misaligned  */
+#define NVFP4_ERR_WORKSPACE 4  /* workspace missing, too small or misaligned */
+#define NVFP4_ERR_CUDA 5       /* a kernel launch failed                     */
+#define NVFP4_ERR_TIMEOUT 6    /* device: a bounded wait gave up             */
+#define NVFP4_ERR_NONFINITE 7  /* device: Inf/NaN in the quantiser's input   */
+#define NVFP4_ERR_DTYPE 8      /* unknown output dtype                       */
+
+/* Output element types. */
+#define NVFP4_DTYPE_F32 0
+#define NVFP4_DTYPE_BF16 1
+
+/* Largest activation batch of the GEMV calls (one MMA column per row). */
+#define W4A16_GEMV_MAX_M 8
+/* Largest total K of the GEMV calls (activations are staged on chip). */
+#define W4A16_GEMV_MAX_K 16384
+/* Workspace of w4a16_gemv_argmax: W4A16_GEMV_MAX_M 64-bit keys + a counter.
+ * Zero it once when allocated; every completed call leaves it zeroed. */
+#define W4A16_ARGMAX_WS_BYTES 128
+/* Workspace of nvfp4_quantize when its absmax output is NULL. */
+#define NVFP4_QUANTIZE_WS_BYTES 16
+
+/* A quantised weight (all device pointers, 16-byte aligned). */
+typedef struct nvfp4_weight {
+    const uint8_t *packed;       /* [n, k/2] E2M1 codes                */
+    const uint8_t *scales;       /* [n, k/16] E4M3 block scales        */
+    const float *global_scale;   /* 1 float: g                         */
+    int64_t n;                   /* output features (rows)             */
+    int64_t k;                   /* input features, multiple of 32     */
+} nvfp4_weight;
+
+/* One activation segment of the GEMV input.  The GEMV input row m is the
+ * concatenation, in argument order, of every segment's row m, each optionally
+ * RMS-normalised first:
+ *     a = bf16( x * (1 / sqrt(mean(x^2) + eps)) * gamma )     (gamma != NULL)
+ *     a = x                                                   (gamma == NULL)
+ * with gamma applied as stored (the "vanilla" RMSNorm of the draft head in
+ * "spark_model/layers/deepseek_v4_mtp.rs", constructor) and the embedding
+ * segment first for the fc combiner (pre-fc norms, concat, fc, as the module
+ * doc of "metrale_model_layers/layers/mtp_head.rs" orders the draft step). */
+typedef struct w4a16_act_segment {
+    const void *x;      /* BF16 [m, k_seg], row stride ld elements, 16-B aligned */
+    int64_t k_seg;      /* multiple of 32                                         */
+    int64_t ld;         /* row stride in elements, multiple of 8, >= k_seg        */
+    const void *gamma;  /* BF16 [k_seg], 16-B aligned, or NULL for no norm        */
+    float eps;
+} w4a16_act_segment;
+
+/* Execution context. */
+typedef struct nvfp4_exec {
+    void *stream;           /* cudaStream_t                                  */
+    void *workspace;        /* device, 16-byte aligned, see each call        */
+    size_t workspace_bytes;
+    int32_t *dev_status;    /* nullable device int32, see above              */
+} nvfp4_exec;
+
+/*
+ * nvfp4_quantize -- load-time BF16 -> NVFP4 quantisation of w[n, k].
+ * The two passes of the load path in "spark_model/layers/mtp_head/new.rs"
+ * (MtpHead::new: the global-absmax kernel, then the BF16->NVFP4 kernel):
+ *   amax = max |w|;  g = fl32(amax / 2688)
+ *   per 16-block b of a row: s_b = E4M3_rne_satfinite(fl32(amax_b / fl32(6 g)))
+ *                            (s_b = 0 when g == 0 or amax_b == 0)
+ *   per element: d = fl32(e4m3(s_b) * g);
+ *                code = d == 0 ? +0 : E2M1_rne_satfinite(fl32(x / d)) with the
+ *                sign bit of x.
+ *   w_bf16       device BF16 [n, k] row-major, 16-byte aligned.
+ *   n >= 1, k >= 32, k % 32 == 0.
+ *   packed       device uint8 [n, k/2] (16-byte aligned), written.
+ *   scales       device uint8 [n, k/16], written.
+ *   global_scale device float, written with g.
+ *   absmax       device float or NULL; written with amax.  When NULL the
+ *                workspace must hold NVFP4_QUANTIZE_WS_BYTES.
+ * Non-finite input: results undefined, NVFP4_ERR_NONFINITE to dev_status.
+ */
+int nvfp4_quantize(const void *w_bf16, int64_t n, int64_t k, uint8_t *packed,
+                   uint8_t *scales, float *global_scale, float *absmax,
+                   const nvfp4_exec *ex);
+
+/*
+ * w4a16_gemv -- batched W4A16 GEMV, y[m, n] = g * sum_i a[m, i] * w~[n, i],
+ * where w~ = e4m3(s) * e2m1(c) is exact in BF16 and the sum is accumulated in
+ * FP32; the global scale multiplies the finished sum.  This is the NVFP4 arm
+ * of the per-precision one-row GEMV of "metrale_model_layers/layers/mtp_head.rs"
+ * (MtpHead::gemv -> w4a16_decode_gemv), batched to m <= 8 rows and with the
+ * draft head's RMSNorm + concat fused into the activation load.
+ *   seg, nseg     host array of 1 or 2 segments; sum of k_seg == w->k.
+ *   m             1..W4A16_GEMV_MAX_M activation rows.
+ *   w             host struct describing the weight; w->k <= W4A16_GEMV_MAX_K.
+ *   y             device [m, ldy] of y_dtype (F32 or BF16, round-to-nearest-even),
+ *                 ldy >= w->n.
+ * Workspace: none.
+ */
+int w4a16_gemv(const w4a16_act_segment *seg, int nseg, int m, const nvfp4_weight *w,
+               void *y, int y_dtype, int64_t ldy, const nvfp4_exec *ex);
+
+/*
+ * w4a16_gemv_argmax -- the same GEMV with greedy argmax fused on the output:
+ * argmax[r] = the lowest index n with y[r, n] maximal over the FP32 logits,
+ * the scan of "spark_model/layers/deepseek_v4_mtp.rs" (argmax_grammar_masked:
+ * strict '>' ascending from -inf, so NaN never wins and 0 comes back when no
+ * logit exceeds -inf), applied to the reduced-vocab LM head's rows.
+ *   logits        device float [m, ld_logits] or NULL (not written).
+ *   argmax        device int32 [m].
+ * Workspace: W4A16_ARGMAX_WS_BYTES, 16-byte aligned, zeroed once by the caller
+ * when allocated; each completed call returns it to zero.
+ */
+int w4a16_gemv_argmax(const w4a16_act_segment *seg, int nseg, int m,
+                      const nvfp4_weight *w, float *logits, int64_t ld_logits,
+                      int32_t *argmax, const nvfp4_exec *ex);
+
+/*
+ * w4a16_gemm -- prefill W4A16 GEMM, C[m, n] = bf16( g * A[m, :] . w~[n, :] ),
+ * w~ dequantised exactly to BF16 and multiplied with BF16 tensor-core MMAs
+ * accumulating in FP32, in 128-row tiles of A.  This is the lossless
+ * "FP4->BF16 dequant + BF16 MMA" numerics of the M=128 prefill GEMM dispatch in
+ * "spark_model/layers/qwen3_attention/prefill_weights.rs"
+ * (w4a16_gemm_m128_dispatch, BF16 tensor-core variant).
+ *   a_bf16   device BF16 [m, lda], 16-byte aligned, lda % 8 == 0, lda >= k.
+ *   m >= 1 (any; the last tile is masked); w->n % 128 == 0; w->k % 64 == 0.
+ *   c_bf16   device BF16 [m, ldc], 16-byte aligned, ldc % 8 == 0, ldc >= n.
+ * Workspace: none.
+ */
+int w4a16_gemm(const void *a_bf16, int64_t m, int64_t lda, const nvfp4_weight *w,
+               void *c_bf16, int64_t ldc, const nvfp4_exec *ex);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NVFP4DRAFT_H */

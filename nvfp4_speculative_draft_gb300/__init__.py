@@ -1,0 +1,218 @@
+"""Python binding of the NVFP4 W4A16 projection library (sm_103a).
+
+Argument marshalling only: every step of the hot path runs in the CUDA
+library ``_build/libnvfp4draft.so`` behind the C ABI of
+``include/nvfp4draft.h``.  PyTorch supplies device memory and streams.  If
+the library has not been built, :func:`load` raises -- there is no CPU
+fallback.
+
+The four calls keep the C names:
+
+* :func:`nvfp4_quantize`     BF16 [n, k] -> NVFP4 (packed, scales, g, absmax)
+* :func:`w4a16_gemv`         y[m, n] = g * a . w~   (m <= 8, RMSNorm/concat fused)
+* :func:`w4a16_gemv_argmax`  the same, FP32 logits + fused greedy argmax
+* :func:`w4a16_gemm`         prefill C[m, n] = bf16(g * A . w~^T)
+"""
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Optional, Sequence
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_build", "libnvfp4draft.so")
+
+NVFP4_OK = 0
+STATUS_NAMES = {0: "OK", 1: "ERR_NULL", 2: "ERR_SHAPE", 3: "ERR_ALIGN", 4: "ERR_WORKSPACE",
+                5: "ERR_CUDA", 6: "ERR_TIMEOUT", 7: "ERR_NONFINITE", 8: "ERR_DTYPE"}
+DTYPE_F32 = 0
+DTYPE_BF16 = 1
+GEMV_MAX_M = 8
+GEMV_MAX_K = 16384
+ARGMAX_WS_BYTES = 128
+QUANTIZE_WS_BYTES = 16
+EXPORTED = ("nvfp4_quantize", "w4a16_gemv", "w4a16_gemv_argmax", "w4a16_gemm")
+
+
+class Nvfp4Error(RuntimeError):
+    def __init__(self, call, status):
+        super().__init__(f"{call} failed: {STATUS_NAMES.get(status, status)}")
+        self.status = status
+
+
+class _Weight(ctypes.Structure):
+    _fields_ = [("packed", ctypes.c_void_p), ("scales", ctypes.c_void_p),
+                ("global_scale", ctypes.c_void_p), ("n", ctypes.c_int64), ("k", ctypes.c_int64)]
+
+
+class _Segment(ctypes.Structure):
+    _fields_ = [("x", ctypes.c_void_p), ("k_seg", ctypes.c_int64), ("ld", ctypes.c_int64),
+                ("gamma", ctypes.c_void_p), ("eps", ctypes.c_float)]
+
+
+class _Exec(ctypes.Structure):
+    _fields_ = [("stream", ctypes.c_void_p), ("workspace", ctypes.c_void_p),
+                ("workspace_bytes", ctypes.c_size_t), ("dev_status", ctypes.c_void_p)]
+
+
+_LIB = None
+
+
+def load(path: str = LIB_PATH):
+    """Load the CUDA library (raises if it was not built)."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    if not os.path.exists(path):
+        raise ImportError(f"NVFP4 CUDA library not built: {path} is missing "
+                          "(run __graft_entry__.build() or python -m "
+                          "nvfp4_speculative_draft_gb300.build)")
+    L = ctypes.CDLL(path)
+    vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+    P = ctypes.POINTER
+    L.nvfp4_quantize.argtypes = [vp, i64, i64, vp, vp, vp, vp, P(_Exec)]
+    L.w4a16_gemv.argtypes = [P(_Segment), i32, i32, P(_Weight), vp, i32, i64, P(_Exec)]
+    L.w4a16_gemv_argmax.argtypes = [P(_Segment), i32, i32, P(_Weight), vp, i64, vp, P(_Exec)]
+    L.w4a16_gemm.argtypes = [vp, i64, i64, P(_Weight), vp, i64, P(_Exec)]
+    for f in EXPORTED:
+        getattr(L, f).restype = ctypes.c_int
+    _LIB = L
+    return L
+
+
+@dataclass
+class Nvfp4Weight:
+    """Device tensors of one quantised weight."""
+    packed: torch.Tensor   # uint8 [n, k/2]
+    scales: torch.Tensor   # uint8 [n, k/16]
+    global_scale: torch.Tensor  # float32 [1]
+    n: int
+    k: int
+
+    def c(self) -> _Weight:
+        return _Weight(self.packed.data_ptr(), self.scales.data_ptr(),
+                       self.global_scale.data_ptr(), self.n, self.k)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _exec(stream=None, workspace: Optional[torch.Tensor] = None,
+          dev_status: Optional[torch.Tensor] = None) -> _Exec:
+    return _Exec(_stream(stream),
+                 workspace.data_ptr() if workspace is not None else None,
+                 workspace.numel() * workspace.element_size() if workspace is not None else 0,
+                 dev_status.data_ptr() if dev_status is not None else None)
+
+
+_WS = {}
+
+
+def argmax_workspace(device) -> torch.Tensor:
+    """A zeroed argmax workspace per device (each completed call re-zeroes it).
+    Calls on concurrent streams must pass their own workspace instead."""
+    device = torch.device(device)
+    key = ("argmax", device.index)
+    if key not in _WS:
+        _WS[key] = torch.zeros(ARGMAX_WS_BYTES, dtype=torch.uint8, device=device)
+    return _WS[key]
+
+
+def _check(call, rc):
+    if rc != NVFP4_OK:
+        raise Nvfp4Error(call, rc)
+
+
+def nvfp4_quantize(w: torch.Tensor, out: Optional[Nvfp4Weight] = None, absmax: Optional[torch.Tensor] = None,
+                   stream=None, dev_status: Optional[torch.Tensor] = None):
+    """Quantise a BF16 [n, k] device matrix.  Returns (Nvfp4Weight, absmax tensor)."""
+    assert w.dtype == torch.bfloat16 and w.dim() == 2 and w.is_contiguous() and w.is_cuda
+    n, k = w.shape
+    if out is None:
+        out = Nvfp4Weight(torch.empty((n, k // 2), dtype=torch.uint8, device=w.device),
+                          torch.empty((n, k // 16), dtype=torch.uint8, device=w.device),
+                          torch.empty(1, dtype=torch.float32, device=w.device), n, k)
+    if absmax is None:
+        absmax = torch.empty(1, dtype=torch.float32, device=w.device)
+    ex = _exec(stream, None, dev_status)
+    rc = load().nvfp4_quantize(w.data_ptr(), n, k, out.packed.data_ptr(), out.scales.data_ptr(),
+                               out.global_scale.data_ptr(), absmax.data_ptr(), ctypes.byref(ex))
+    _check("nvfp4_quantize", rc)
+    return out, absmax
+
+
+def _segments(segments: Sequence) -> tuple:
+    """segments: [(x [m, k_seg] bf16, gamma [k_seg] bf16 or None, eps), ...]"""
+    arr = (_Segment * len(segments))()
+    m = None
+    for i, s in enumerate(segments):
+        s = tuple(s)
+        x = s[0]
+        gamma = s[1] if len(s) > 1 else None
+        eps = s[2] if len(s) > 2 else 1e-6
+        assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1 and x.is_cuda
+        if gamma is not None:
+            assert gamma.dtype == torch.bfloat16 and gamma.is_contiguous()
+        arr[i] = _Segment(x.data_ptr(), x.shape[1], x.stride(0),
+                          gamma.data_ptr() if gamma is not None else None, float(eps))
+        m = x.shape[0] if m is None else m
+        assert x.shape[0] == m
+    return arr, m
+
+
+def w4a16_gemv(segments: Sequence, weight: Nvfp4Weight, out_dtype=torch.float32,
+               out: Optional[torch.Tensor] = None, stream=None,
+               dev_status: Optional[torch.Tensor] = None) -> torch.Tensor:
+    segs, m = _segments(segments)
+    if out is None:
+        out = torch.empty((m, weight.n), dtype=out_dtype, device=weight.packed.device)
+    dt = DTYPE_F32 if out.dtype == torch.float32 else DTYPE_BF16
+    assert out.dtype in (torch.float32, torch.bfloat16) and out.stride(1) == 1
+    ex = _exec(stream, None, dev_status)
+    w = weight.c()
+    rc = load().w4a16_gemv(segs, len(segments), m, ctypes.byref(w), out.data_ptr(), dt,
+                           out.stride(0), ctypes.byref(ex))
+    _check("w4a16_gemv", rc)
+    return out
+
+
+def w4a16_gemv_argmax(segments: Sequence, weight: Nvfp4Weight, logits: bool = True,
+                      out_logits: Optional[torch.Tensor] = None,
+                      out_argmax: Optional[torch.Tensor] = None,
+                      workspace: Optional[torch.Tensor] = None, stream=None,
+                      dev_status: Optional[torch.Tensor] = None):
+    """Returns (logits FP32 [m, n] or None, argmax int32 [m])."""
+    segs, m = _segments(segments)
+    dev = weight.packed.device
+    if logits and out_logits is None:
+        out_logits = torch.empty((m, weight.n), dtype=torch.float32, device=dev)
+    if out_argmax is None:
+        out_argmax = torch.empty(m, dtype=torch.int32, device=dev)
+    if workspace is None:
+        workspace = argmax_workspace(dev)
+    ex = _exec(stream, workspace, dev_status)
+    w = weight.c()
+    rc = load().w4a16_gemv_argmax(segs, len(segments), m, ctypes.byref(w),
+                                  out_logits.data_ptr() if out_logits is not None else None,
+                                  out_logits.stride(0) if out_logits is not None else 0,
+                                  out_argmax.data_ptr(), ctypes.byref(ex))
+    _check("w4a16_gemv_argmax", rc)
+    return out_logits, out_argmax
+
+
+def w4a16_gemm(a: torch.Tensor, weight: Nvfp4Weight, out: Optional[torch.Tensor] = None,
+               stream=None, dev_status: Optional[torch.Tensor] = None) -> torch.Tensor:
+    assert a.dtype == torch.bfloat16 and a.dim() == 2 and a.stride(1) == 1 and a.is_cuda
+    m = a.shape[0]
+    if out is None:
+        out = torch.empty((m, weight.n), dtype=torch.bfloat16, device=a.device)
+    ex = _exec(stream, None, dev_status)
+    w = weight.c()
+    rc = load().w4a16_gemm(a.data_ptr(), m, a.stride(0), ctypes.byref(w), out.data_ptr(),
+                           out.stride(0), ctypes.byref(ex))
+    _check("w4a16_gemm", rc)
+    return out

@@ -1,0 +1,42 @@
+// common.cuh -- small shared pieces of the CUDA library (status codes come from
+// the public header; nothing here is shared with the CPU oracle).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "nvfp4draft.h"
+
+namespace nvfp4 {
+
+// Record a device-detected condition in the caller's status word (if any).
+__device__ __forceinline__ void report(int32_t* dev_status, int32_t code) {
+  if (dev_status != nullptr) atomicCAS(reinterpret_cast<int*>(dev_status), 0, code);
+}
+
+__host__ __device__ __forceinline__ int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Number of SMs of the current device (cached per device ordinal).
+int sm_count();
+
+// Resident CTAs per SM of `func` at `threads` threads and `smem` dynamic shared
+// bytes on the current device.  The first query per (device, func, smem) raises
+// the function's dynamic shared memory limit to the device maximum and asks the
+// runtime; later queries are served from a table, so calls made while a stream
+// is being captured into a CUDA graph issue no CUDA API calls here.
+int occupancy(const void* func, int threads, size_t smem);
+
+}  // namespace nvfp4
+
+// Launchers implemented in the kernel translation units.
+int launch_quantize(const void* w, int64_t n, int64_t k, uint8_t* packed, uint8_t* scales,
+                    float* global_scale, uint32_t* amax_word, int32_t* dev_status,
+                    cudaStream_t stream);
+int launch_gemv(const w4a16_act_segment* seg, int nseg, int m, const nvfp4_weight* w,
+                void* y, int y_dtype, int64_t ldy, bool want_argmax, int32_t* argmax,
+                void* workspace, int32_t* dev_status, cudaStream_t stream);
+int launch_gemm(const void* a, int64_t m, int64_t lda, const nvfp4_weight* w, void* c,
+                int64_t ldc, int32_t* dev_status, cudaStream_t stream);

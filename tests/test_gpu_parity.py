@@ -1,0 +1,295 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle.
+
+Bar (stated per test):
+  * packed codes, scale bytes, absmax, g: bit-exact;
+  * FP32 logits: |gpu - oracle| <= 1e-3 * S + 1e-6, S = sum |a_i w_i|;
+  * BF16 outputs: the same plus one BF16 ulp of the oracle value;
+  * argmax: equal to the first maximum of the GPU's own FP32 logits (same
+    precision), and equal to the oracle's index whenever the oracle's top-2
+    gap exceeds both tolerances, else inside the oracle's near-max set.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+TOL_REL, TOL_ABS = 1e-3, 1e-6
+
+
+def nd():
+    import nvfp4_speculative_draft_gb300 as m
+    return m
+
+
+def upload_weight(packed, scales, g, dev):
+    m = nd()
+    n, kh = packed.shape
+    return m.Nvfp4Weight(torch.from_numpy(packed).to(dev), torch.from_numpy(scales).to(dev),
+                         torch.tensor([g], dtype=torch.float32, device=dev), n, kh * 2)
+
+
+def quantize_both(w_bf16, dev):
+    """GPU quantisation checked bit-exact against the oracle's."""
+    m = nd()
+    wq, amax = m.nvfp4_quantize(w_bf16.to(dev).contiguous())
+    p, s, g, a = oracle.quantize(workloads.bits(w_bf16))
+    torch.cuda.synchronize()
+    assert amax.item() == float(a), "absmax differs"
+    assert wq.global_scale.item() == float(g), "global scale differs"
+    gp, gs = wq.packed.cpu().numpy(), wq.scales.cpu().numpy()
+    if not np.array_equal(gs, s):
+        bad = np.argwhere(gs != s)[:5]
+        raise AssertionError(f"scale bytes differ at {bad.tolist()}: gpu {gs[tuple(bad[0])]} "
+                             f"oracle {s[tuple(bad[0])]}")
+    if not np.array_equal(gp, p):
+        bad = np.argwhere(gp != p)[:5]
+        raise AssertionError(f"packed codes differ at {bad.tolist()}")
+    return wq, (p, s, g)
+
+
+def oracle_input(segments, eps_default=1e-6):
+    m = segments[0][0].shape[0]
+    return oracle.rmsnorm_concat(
+        [(workloads.bits(x), None if gm is None else workloads.bits(gm), eps_default)
+         for x, gm in segments], m)
+
+
+def check_logits(got, y, sabs):
+    err = np.abs(got.astype(np.float64) - y)
+    tol = TOL_REL * sabs + TOL_ABS
+    bad = np.argwhere(err > tol)
+    assert bad.size == 0, (f"{len(bad)} logits out of tolerance, first {bad[0].tolist()}: "
+                           f"gpu {got[tuple(bad[0])]} oracle {y[tuple(bad[0])]} tol {tol[tuple(bad[0])]}")
+
+
+def check_argmax(idx, logits_gpu, y, sabs):
+    tol = TOL_REL * sabs + TOL_ABS
+    for r in range(y.shape[0]):
+        i = int(idx[r])
+        assert i == oracle.argmax(logits_gpu[r].astype(np.float64)), "not the first max of GPU logits"
+        j = oracle.argmax(y[r])
+        order = np.argsort(-y[r], kind="stable")
+        second = order[1] if order[0] == j else order[0]
+        if y[r, j] - y[r, second] > tol[r, j] + tol[r, second]:
+            assert i == j, f"row {r}: gpu argmax {i}, oracle {j}"
+        else:
+            assert y[r, i] >= y[r, j] - tol[r, j] - tol[r, i]
+
+
+def run_gemv_case(case, dev, m_rows=None, with_bf16=False):
+    m = nd()
+    p, s, g, _ = oracle.quantize(workloads.bits(case.w))
+    wq = upload_weight(p, s, g, dev)
+    segs = [(x if m_rows is None else x[:m_rows], gm) for x, gm in case.segments]
+    a = oracle_input(segs, case.eps)
+    y, sabs = oracle.gemv(a, p, s, g)
+    dsegs = [(x.to(dev), None if gm is None else gm.to(dev), case.eps) for x, gm in segs]
+    logits, idx = m.w4a16_gemv_argmax(dsegs, wq)
+    y32 = m.w4a16_gemv(dsegs, wq)
+    torch.cuda.synchronize()
+    lg = logits.cpu().numpy()
+    check_logits(lg, y, sabs)
+    assert np.array_equal(y32.cpu().numpy(), lg), "w4a16_gemv and w4a16_gemv_argmax logits differ"
+    check_argmax(idx.cpu().numpy(), lg, y, sabs)
+    if with_bf16:
+        yb = m.w4a16_gemv(dsegs, wq, out_dtype=torch.bfloat16)
+        got = yb.float().cpu().numpy().astype(np.float64)
+        ulp = np.abs(y) * 2.0 ** -8
+        err = np.abs(got - y)
+        assert np.all(err <= TOL_REL * sabs + TOL_ABS + ulp)
+    return lg, idx.cpu().numpy(), y
+
+
+# ---------------------------------------------------------------- quantiser
+
+@pytest.mark.parametrize("n,k", [(256, 512), (1, 32), (3, 96), (37, 160), (129, 4096)])
+def test_quantize_bit_exact_shapes(dev, n, k):
+    quantize_both(workloads.tiny(n=n, k=k).w, dev)
+
+
+def test_quantize_bit_exact_wide_block_range(dev):
+    quantize_both(workloads.propose_m8(n=512, k=1024).w, dev)
+
+
+def test_quantize_outlier_rows(dev):
+    quantize_both(workloads.lm_head_m1(n=1000, k=512, rows=1).w, dev)
+
+
+def test_quantize_special_values(dev):
+    rng = np.random.default_rng(7)
+    x = rng.standard_normal((64, 128)).astype(np.float32) * 0.02
+    x[0, :16] = 0.0                                        # zero block
+    x[1, :] = -0.0                                         # negative zeros
+    x[2, :16] = 1e-30                                      # subnormal-scale block
+    x[3, 16:32] = 1.0                                      # constant block
+    x[4, :] = np.linspace(-5, 5, 128)                      # ties after scaling
+    x[5, 7] = 300.0                                        # dominant element: most scales tiny
+    w = torch.from_numpy(x).to(torch.bfloat16)
+    w.view(torch.int16)[1] = -32768                        # exact -0.0 bit pattern
+    quantize_both(w, dev)
+    quantize_both(torch.zeros((8, 64), dtype=torch.bfloat16), dev)
+    big = torch.full((4, 32), 3.3e38).to(torch.bfloat16)
+    big[1] = -big[1]
+    quantize_both(big, dev)
+
+
+def test_quantize_exactly_representable_round_trip(dev):
+    rng = np.random.default_rng(8)
+    n, k = 16, 64
+    codes = rng.integers(0, 16, size=(n, k))
+    codes.reshape(n, -1, 16)[:, :, 3] = 7
+    sc = rng.integers(0x10, 0x7E, size=(n, k // 16))
+    sc[0, 0] = 0x7E
+    val = np.vectorize(oracle.e2m1_value)(codes) * np.repeat(np.vectorize(oracle.e4m3_value)(sc), 16, 1)
+    w = torch.from_numpy(val * 2.0 ** -12).to(torch.bfloat16)
+    wq, (p, s, g) = quantize_both(w, dev)
+    assert np.array_equal(s, sc.astype(np.uint8))
+
+
+def test_quantize_nonfinite_is_reported(dev):
+    m = nd()
+    w = torch.ones((4, 64), dtype=torch.bfloat16)
+    w[2, 5] = float("inf")
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    m.nvfp4_quantize(w.to(dev), dev_status=status)
+    torch.cuda.synchronize()
+    assert status.item() == 7  # NVFP4_ERR_NONFINITE
+
+
+# --------------------------------------------------------------------- GEMV
+
+@pytest.mark.parametrize("m_rows", [1, 2, 3, 4, 5, 8])
+def test_gemv_small_all_batch_widths(dev, m_rows):
+    run_gemv_case(workloads.propose_m8(n=1000, k=640, m=8), dev, m_rows=m_rows)
+
+
+@pytest.mark.parametrize("n,k", [(16, 32), (17, 64), (100, 96), (257, 224), (2003, 1056)])
+def test_gemv_ragged_shapes(dev, n, k):
+    run_gemv_case(workloads.propose_m8(n=n, k=k, m=3), dev, with_bf16=True)
+
+
+def test_gemv_tiny_config(dev):
+    run_gemv_case(workloads.tiny(), dev)
+
+
+def test_gemv_rmsnorm_fused(dev):
+    run_gemv_case(workloads.lm_head_m1(n=3000, k=1024, rows=4), dev)
+
+
+def test_gemv_two_segment_concat_bf16_out(dev):
+    run_gemv_case(workloads.fc_combiner(n=640, k_seg=512, m=5), dev, with_bf16=True)
+
+
+def test_gemv_strided_activations(dev):
+    m = nd()
+    case = workloads.propose_m8(n=300, k=256, m=4)
+    p, s, g, _ = oracle.quantize(workloads.bits(case.w))
+    wq = upload_weight(p, s, g, dev)
+    x = case.segments[0][0]
+    big = torch.zeros((4, 264), dtype=torch.bfloat16)
+    big[:, :256] = x
+    y, sabs = oracle.gemv(workloads.bits(x), p, s, g)
+    out = torch.full((4, 320), float("nan"), device=dev)
+    m.w4a16_gemv([(big.to(dev)[:, :256], None)], wq, out=out[:, :300])
+    torch.cuda.synchronize()
+    o = out.cpu().numpy()
+    check_logits(o[:, :300], y, sabs)
+    assert np.all(np.isnan(o[:, 300:])), "wrote outside the output rows"
+
+
+def test_argmax_ties_pick_lowest_index(dev):
+    m = nd()
+    case = workloads.propose_m8(n=700, k=256, m=2)
+    p, s, g, _ = oracle.quantize(workloads.bits(case.w))
+    x = case.segments[0][0]
+    y, _ = oracle.gemv(workloads.bits(x), p, s, g)
+    for r in range(2):
+        j = oracle.argmax(y[r])
+        lo = 5 if j > 5 else j + 1
+        hi = 650 if j < 650 else j - 1
+        p2, s2 = p.copy(), s.copy()
+        for tgt in (lo, hi):
+            p2[tgt], s2[tgt] = p[j], s[j]
+        wq = upload_weight(p2, s2, g, dev)
+        logits, idx = m.w4a16_gemv_argmax([(x.to(dev), None)], wq)
+        torch.cuda.synchronize()
+        lg = logits.cpu().numpy()
+        assert lg[r, lo] == lg[r, j] == lg[r, hi], "duplicated rows must give bit-equal logits"
+        assert idx[r].item() == min(lo, j, hi)
+
+
+def test_argmax_workspace_returns_to_zero_and_repeats(dev):
+    m = nd()
+    case = workloads.tiny(n=512, k=256, m=3)
+    p, s, g, _ = oracle.quantize(workloads.bits(case.w))
+    wq = upload_weight(p, s, g, dev)
+    ws = torch.zeros(m.ARGMAX_WS_BYTES, dtype=torch.uint8, device=dev)
+    x = case.segments[0][0].to(dev)
+    outs = []
+    for _ in range(3):
+        _, idx = m.w4a16_gemv_argmax([(x, None)], wq, logits=False, workspace=ws)
+        outs.append(idx.cpu().numpy())
+    torch.cuda.synchronize()
+    assert not ws.any().item()
+    assert all(np.array_equal(o, outs[0]) for o in outs)
+    y, sabs = oracle.gemv(workloads.bits(case.segments[0][0]), p, s, g)
+    logits, _ = m.w4a16_gemv_argmax([(x, None)], wq, workspace=ws)
+    torch.cuda.synchronize()
+    check_argmax(outs[0], logits.cpu().numpy(), y, sabs)
+
+
+def test_argmax_all_negative_infinity_and_nan_logits(dev):
+    # a zero weight gives y = 0 everywhere: the first index wins
+    m = nd()
+    wq = upload_weight(np.zeros((64, 32), np.uint8), np.zeros((64, 4), np.uint8), 1.0, dev)
+    x = torch.ones((1, 64), dtype=torch.bfloat16, device=dev)
+    _, idx = m.w4a16_gemv_argmax([(x, None)], wq, logits=False)
+    torch.cuda.synchronize()
+    assert idx.item() == 0
+
+
+# --------------------------------------------------------------------- GEMM
+
+def check_gemm(a, wq_oracle, c_gpu, rows, cols):
+    p, s, g = wq_oracle
+    exact, sabs = oracle.gemm_pairs(workloads.bits(a), p, s, g, rows, cols)
+    got = c_gpu[rows, cols].astype(np.float64)
+    ulp = np.abs(exact) * 2.0 ** -8
+    err = np.abs(got - exact)
+    bad = np.nonzero(err > TOL_REL * sabs + TOL_ABS + ulp)[0]
+    assert bad.size == 0, f"{bad.size} outputs off, first ({rows[bad[0]]},{cols[bad[0]]}): " \
+                          f"gpu {got[bad[0]]} oracle {exact[bad[0]]}"
+
+
+@pytest.mark.parametrize("m_rows,n,k", [(128, 128, 64), (200, 256, 320), (1, 384, 128),
+                                        (257, 128, 1024)])
+def test_gemm_small_all_outputs(dev, m_rows, n, k):
+    m = nd()
+    case = workloads.prefill_gemm(m=m_rows, n=n, k=k)
+    p, s, g, _ = oracle.quantize(workloads.bits(case.w))
+    wq = upload_weight(p, s, g, dev)
+    c = m.w4a16_gemm(case.a.to(dev), wq)
+    torch.cuda.synchronize()
+    cg = c.float().cpu().numpy()
+    rows = np.repeat(np.arange(m_rows), n)
+    cols = np.tile(np.arange(n), m_rows)
+    check_gemm(case.a, (p, s, g), cg, rows, cols)
+
+
+def test_gemm_strided_output(dev):
+    m = nd()
+    case = workloads.prefill_gemm(m=130, n=256, k=192)
+    p, s, g, _ = oracle.quantize(workloads.bits(case.w))
+    wq = upload_weight(p, s, g, dev)
+    out = torch.full((130, 264), float("nan"), dtype=torch.bfloat16, device=dev)
+    m.w4a16_gemm(case.a.to(dev), wq, out=out[:, :256])
+    torch.cuda.synchronize()
+    o = out.float().cpu().numpy()
+    assert np.all(np.isnan(o[:, 256:]))
+    rows = np.repeat(np.arange(130), 256)
+    cols = np.tile(np.arange(256), 130)
+    check_gemm(case.a, (p, s, g), o, rows, cols)
