@@ -42,8 +42,11 @@ int occupancy(const void* func, int threads, size_t smem) {
   int maxopt = 0;
   if (cudaDeviceGetAttribute(&maxopt, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
     return 0;
-  if (smem > (size_t)maxopt) return 0;
-  if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, maxopt) != cudaSuccess)
+  cudaFuncAttributes attr;
+  if (cudaFuncGetAttributes(&attr, func) != cudaSuccess) return 0;
+  const int limit = maxopt - (int)attr.sharedSizeBytes;  // dynamic + static <= opt-in maximum
+  if (limit < 0 || smem > (size_t)limit) return 0;
+  if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, limit) != cudaSuccess)
     return 0;
   int occ = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, func, threads, smem) != cudaSuccess)
