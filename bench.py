@@ -192,12 +192,11 @@ def bench_lm_head(args, dev, dist_on, stream):
             nd.w4a16_gemv_argmax([(h[r:r + 1], gamma, 1e-6)], weights[r % copies], logits=False,
                                  out_argmax=out_idx[r:r + 1], workspace=ws, stream=stream)
 
-    with torch.cuda.stream(stream):
-        step()  # warm the library (occupancy queries, attributes) before capture
-        torch.cuda.synchronize()
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph, stream=stream, capture_error_mode="thread_local"):
-            step()
+    step()  # warm the library (occupancy queries, attributes) before capture
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream, capture_error_mode="thread_local"):
+        step()
     for _ in range(args.warmup):
         graph.replay()
     barrier(dist_on)
@@ -229,16 +228,21 @@ def bench_lm_head(args, dev, dist_on, stream):
                                  stream=stream)
         idx_host.copy_(out_idx, non_blocking=True)
 
-    with torch.cuda.stream(stream):
-        for _ in range(2):
-            e2e_step()
-        torch.cuda.synchronize()
-        e2e_steps = max(1, min(args.steps, 5))
-        t0 = time.perf_counter()
-        for _ in range(e2e_steps):
-            e2e_step()
-        stream.synchronize()
-        e2e_ms = (time.perf_counter() - t0) * 1e3 / e2e_steps
+    e2e_step()
+    torch.cuda.synchronize()
+    g2 = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g2, stream=stream, capture_error_mode="thread_local"):
+        e2e_step()
+    for _ in range(args.warmup):
+        g2.replay()
+    torch.cuda.synchronize()
+    e2e_steps = max(3, min(args.steps, 20))
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        g2.replay()
+        stream.synchronize()      # the host needs the token ids of this step
+        _ = int(idx_host[0])
+    e2e_ms = (time.perf_counter() - t0) * 1e3 / e2e_steps
     e2e_ms = max_over_ranks(e2e_ms, dist_on)
     return {
         "ms_step": ms_step, "calls": rows, "bytes_per_call": per_call, "copies": copies,
@@ -248,12 +252,14 @@ def bench_lm_head(args, dev, dist_on, stream):
 
 
 def time_graph(fn, stream, iters, warmup=3):
-    with torch.cuda.stream(stream):
+    """Capture fn (launches on `stream`, the current stream) in a CUDA graph and
+    time `iters` replays with events on that stream."""
+    assert torch.cuda.current_stream() == stream
+    fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
         fn()
-        torch.cuda.synchronize()
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
-            fn()
     for _ in range(warmup):
         g.replay()
     torch.cuda.synchronize()
@@ -262,7 +268,9 @@ def time_graph(fn, stream, iters, warmup=3):
     for _ in range(iters):
         g.replay()
     t.stop()
-    return t.ms() / iters
+    ms = t.ms() / iters
+    torch.cuda.synchronize()
+    return ms
 
 
 def bench_details(dev, stream, hbm, bf16):
@@ -404,6 +412,9 @@ def main():
     __graft_entry__.build()
     hbm, bf16, bf16_sus, src = peaks()
     stream = torch.cuda.Stream(device=dev)
+    # Every allocation, launch and graph replay of the run goes to this one
+    # stream, so the caching allocator's stream order covers all of them.
+    torch.cuda.set_stream(stream)
     r = bench_lm_head(args, dev, dist_on, stream)
     gbps = r["calls"] * r["bytes_per_call"] / (r["ms_step"] * 1e-3) / 1e9 * world
     per_launch_us = r["ms_step"] * 1e3 / r["calls"]

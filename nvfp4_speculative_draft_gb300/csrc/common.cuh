@@ -15,6 +15,20 @@ __device__ __forceinline__ void report(int32_t* dev_status, int32_t code) {
   if (dev_status != nullptr) atomicCAS(reinterpret_cast<int*>(dev_status), 0, code);
 }
 
+// Debug builds (-DNVFP4_DEBUG_BOUNDS) check every global and shared access of
+// the kernels against the extents its arguments imply; a failed check records
+// 1000 + tag in the caller's status word and the access is skipped.  Release
+// builds compile the checks away.
+#ifdef NVFP4_DEBUG_BOUNDS
+__device__ __forceinline__ bool guard(bool ok, int tag, int32_t* st) {
+  if (!ok) report(st, 1000 + tag);
+  return ok;
+}
+#define NVFP4_GUARD(cond, tag, st) (::nvfp4::guard((cond), (tag), (st)))
+#else
+#define NVFP4_GUARD(cond, tag, st) true
+#endif
+
 __host__ __device__ __forceinline__ int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }

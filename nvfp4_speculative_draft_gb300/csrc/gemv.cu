@@ -120,7 +120,10 @@ __device__ __forceinline__ uint32_t e2m1_pair(uint32_t x, uint32_t mul) {
 // scale pairs sg / sh, B fragments from shared memory.
 __device__ __forceinline__ void chunk_mma(float (&acc)[4], const uint4& qg, const uint4& qh,
                                           uint32_t sg, uint32_t sh, const uint2* bfrag,
-                                          int bstride, bool bact) {
+                                          int bstride, bool bact, int64_t bleft,
+                                          int32_t* dev_status) {
+  (void)bleft;
+  (void)dev_status;
   uint32_t Sg[2], Sh[2];
   decode_scales(sg, Sg[0], Sg[1]);
   decode_scales(sh, Sh[0], Sh[1]);
@@ -140,10 +143,11 @@ __device__ __forceinline__ void chunk_mma(float (&acc)[4], const uint4& qg, cons
     const uint32_t ah2 = bf16x2_mul(e2m1_pair(h8 & 0x000F000Fu, 0x1040u), sH);
     const uint32_t ah3 = bf16x2_mul(e2m1_pair(h8 & 0x00F000F0u, 0x0104u), sH);
     uint2 b = make_uint2(0u, 0u);
-    if (bact) b = bfrag[(2 * w) * bstride];
+    if (bact && NVFP4_GUARD((2 * w) * bstride < bleft, 7, dev_status)) b = bfrag[(2 * w) * bstride];
     mma_bf16_16816(acc, ag0, ah0, ag1, ah1, b.x, b.y);
     b = make_uint2(0u, 0u);
-    if (bact) b = bfrag[(2 * w + 1) * bstride];
+    if (bact && NVFP4_GUARD((2 * w + 1) * bstride < bleft, 7, dev_status))
+      b = bfrag[(2 * w + 1) * bstride];
     mma_bf16_16816(acc, ag2, ah2, ag3, ah3, b.x, b.y);
   }
 }
@@ -179,6 +183,7 @@ __device__ void build_fragments(const GemvParams& p, uint2* bfrag, float* rms) {
     const __nv_bfloat16* xr = p.x[s] + (int64_t)r * p.ld[s];
     float ss = 0.0f;
     for (int64_t i = (int64_t)lane * 8; i < p.kseg[s]; i += 32 * 8) {
+      if (!NVFP4_GUARD(r < M && s < p.nseg && i + 8 <= p.kseg[s], 1, p.dev_status)) continue;
       const uint4 v = *reinterpret_cast<const uint4*>(xr + i);
       const uint32_t u[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -201,9 +206,9 @@ __device__ void build_fragments(const GemvParams& p, uint2* bfrag, float* rms) {
     const int r = (int)(gi / (kpad / 8));
     const int64_t kk = (gi % (kpad / 8)) * 8;
     uint32_t a[4] = {0u, 0u, 0u, 0u};  // bf16 pairs (a0,a1),(a2,a3),(a4,a5),(a6,a7)
-    if (kk < p.k) {
-      const int s = (p.nseg == 2 && kk >= p.kseg[0]) ? 1 : 0;
-      const int64_t ko = kk - (s ? p.kseg[0] : 0);
+    const int s = (p.nseg == 2 && kk >= p.kseg[0]) ? 1 : 0;
+    const int64_t ko = kk - (s ? p.kseg[0] : 0);
+    if (kk < p.k && NVFP4_GUARD(r < M && ko >= 0 && ko + 8 <= p.kseg[s], 2, p.dev_status)) {
       const uint4 v = *reinterpret_cast<const uint4*>(p.x[s] + (int64_t)r * p.ld[s] + ko);
       a[0] = v.x; a[1] = v.y; a[2] = v.z; a[3] = v.w;
       if (p.gamma[s] != nullptr) {
@@ -221,6 +226,9 @@ __device__ void build_fragments(const GemvParams& p, uint2* bfrag, float* rms) {
     }
     const int c = (int)(kk / kChunk), t = (int)((kk % kChunk) / 32), w = (int)((kk % 32) / 8);
     const int L = 4 * r + t;
+    if (!NVFP4_GUARD((int64_t)(8 * c + 2 * w + 1) * bstride + L < (int64_t)p.nchunks * 8 * bstride &&
+                         L < bstride, 3, p.dev_status))
+      continue;
     // element e of the group lives in half (e & 1) of a[e >> 1]
     const uint32_t e0 = a[0] & 0xFFFFu, e1 = a[0] >> 16, e2 = a[1] & 0xFFFFu, e3 = a[1] >> 16;
     const uint32_t e4 = a[2] & 0xFFFFu, e5 = a[2] >> 16, e6 = a[3] & 0xFFFFu, e7 = a[3] >> 16;
@@ -270,7 +278,13 @@ gemv_kernel(const __grid_constant__ GemvParams p) {
       uint4 qa[kPF], qb[kPF];
       uint32_t sa[kPF], sb[kPF];
       auto load = [&](int i, int c) {
-        const bool kv = c < c_end && (int64_t)c * kChunk + 32 * t < p.k;
+        bool kv = c < c_end && (int64_t)c * kChunk + 32 * t < p.k;
+        kv = kv && NVFP4_GUARD(!v0 || (r0 * rowbytes + 16 * t + (int64_t)c * 64 + 16 <= p.n * rowbytes &&
+                                       r0 * rowscales + 2 * t + 8 * (int64_t)c + 2 <= p.n * rowscales),
+                               4, p.dev_status);
+        kv = kv && NVFP4_GUARD(!v1 || (r1 * rowbytes + 16 * t + (int64_t)c * 64 + 16 <= p.n * rowbytes &&
+                                       r1 * rowscales + 2 * t + 8 * (int64_t)c + 2 <= p.n * rowscales),
+                               5, p.dev_status);
         qa[i] = (kv && v0) ? ld_stream_u4(w0 + (int64_t)c * 64) : make_uint4(0, 0, 0, 0);
         qb[i] = (kv && v1) ? ld_stream_u4(w1 + (int64_t)c * 64) : make_uint4(0, 0, 0, 0);
         sa[i] = (kv && v0) ? (uint32_t)__ldg(s0 + 4 * c) : 0u;
@@ -282,8 +296,9 @@ gemv_kernel(const __grid_constant__ GemvParams p) {
 #pragma unroll
         for (int i = 0; i < kPF; ++i) {
           if (c + i < c_end) {
-            chunk_mma(acc, qa[i], qb[i], sa[i], sb[i], bfrag + (int64_t)(8 * (c + i)) * bstride + lane,
-                      bstride, bact);
+            const int64_t boff = (int64_t)(8 * (c + i)) * bstride + lane;
+            chunk_mma(acc, qa[i], qb[i], sa[i], sb[i], bfrag + boff, bstride, bact,
+                      (int64_t)p.nchunks * 8 * bstride - boff, p.dev_status);
             load(i, c + i + kPF);
           }
         }
@@ -313,7 +328,7 @@ gemv_kernel(const __grid_constant__ GemvParams p) {
           const int mm = 2 * t + e;
           if (mm >= M) continue;
           const float v = acc[2 * h + e] * gs;
-          if (p.y != nullptr) {
+          if (p.y != nullptr && NVFP4_GUARD(mm < M && rows[h] < p.n && rows[h] < p.ldy, 6, p.dev_status)) {
             if (p.y_dtype == NVFP4_DTYPE_F32)
               reinterpret_cast<float*>(p.y)[mm * p.ldy + rows[h]] = v;
             else
