@@ -65,6 +65,7 @@ int check_weight(const nvfp4_weight* w) {
   if (w == nullptr || w->packed == nullptr || w->scales == nullptr || w->global_scale == nullptr)
     return NVFP4_ERR_NULL;
   if (w->n < 1 || w->k < 32 || w->k % 32 != 0) return NVFP4_ERR_SHAPE;
+  if (w->n * (w->k / 2) >= (int64_t)1 << 32) return NVFP4_ERR_SHAPE;  // 32-bit offsets
   if (!aligned16(w->packed) || (reinterpret_cast<uintptr_t>(w->scales) & 1u) ||
       (reinterpret_cast<uintptr_t>(w->global_scale) & 3u))
     return NVFP4_ERR_ALIGN;

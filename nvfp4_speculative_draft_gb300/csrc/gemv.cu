@@ -39,10 +39,10 @@
 
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr int kChunk = 128;  // K elements per lane-group iteration (64 bytes per row)
-constexpr int kPF = 2;       // chunks in flight per lane
+constexpr int kPF = 2;       // chunks in flight per lane (register double buffer)
 
 struct GemvParams {
   const __nv_bfloat16* x[2];
@@ -66,6 +66,7 @@ struct GemvParams {
   int ks;          // warps sharing one 16-row tile (split K)
   int64_t ntiles;  // ceil(n / 16)
   int nchunks;     // ceil(k / 128)
+  int nfull;       // chunks lying entirely inside k (the rest is one tail chunk)
 };
 
 __device__ __forceinline__ uint4 ld_stream_u4(const void* p) {
@@ -117,13 +118,12 @@ __device__ __forceinline__ uint32_t e2m1_pair(uint32_t x, uint32_t mul) {
 }
 
 // One 128-element chunk of one lane: weights qg (row g) / qh (row g + 8),
-// scale pairs sg / sh, B fragments from shared memory.
+// scale pairs sg / sh, B fragments from shared memory at bfrag[j * BSTRIDE]
+// for MMA j (lanes whose batch column is >= M read a duplicate of a valid
+// column: MMA columns are independent and those outputs are discarded).
+template <int BSTRIDE>
 __device__ __forceinline__ void chunk_mma(float (&acc)[4], const uint4& qg, const uint4& qh,
-                                          uint32_t sg, uint32_t sh, const uint2* bfrag,
-                                          int bstride, bool bact, int64_t bleft,
-                                          int32_t* dev_status) {
-  (void)bleft;
-  (void)dev_status;
+                                          uint32_t sg, uint32_t sh, const uint2* bfrag) {
   uint32_t Sg[2], Sh[2];
   decode_scales(sg, Sg[0], Sg[1]);
   decode_scales(sh, Sh[0], Sh[1]);
@@ -142,13 +142,10 @@ __device__ __forceinline__ void chunk_mma(float (&acc)[4], const uint4& qg, cons
     const uint32_t ah1 = bf16x2_mul(e2m1_pair(h0 & 0x00F000F0u, 0x0104u), sH);
     const uint32_t ah2 = bf16x2_mul(e2m1_pair(h8 & 0x000F000Fu, 0x1040u), sH);
     const uint32_t ah3 = bf16x2_mul(e2m1_pair(h8 & 0x00F000F0u, 0x0104u), sH);
-    uint2 b = make_uint2(0u, 0u);
-    if (bact && NVFP4_GUARD((2 * w) * bstride < bleft, 7, dev_status)) b = bfrag[(2 * w) * bstride];
-    mma_bf16_16816(acc, ag0, ah0, ag1, ah1, b.x, b.y);
-    b = make_uint2(0u, 0u);
-    if (bact && NVFP4_GUARD((2 * w + 1) * bstride < bleft, 7, dev_status))
-      b = bfrag[(2 * w + 1) * bstride];
-    mma_bf16_16816(acc, ag2, ah2, ag3, ah3, b.x, b.y);
+    const uint2 b0 = bfrag[(2 * w) * BSTRIDE];
+    mma_bf16_16816(acc, ag0, ah0, ag1, ah1, b0.x, b0.y);
+    const uint2 b1 = bfrag[(2 * w + 1) * BSTRIDE];
+    mma_bf16_16816(acc, ag2, ah2, ag3, ah3, b1.x, b1.y);
   }
 }
 
@@ -169,10 +166,11 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // Fragment layout: MMA index q = 8 * chunk + j, lane L = 4 * m + t (m < M):
 // uint2 at bfrag[q * 4M + L].  For the 8 activations at
 // kk = 128 c + 32 t + 8 w (+0..7):  MMA 8c+2w gets {a0,a4},{a1,a5};
-// MMA 8c+2w+1 gets {a2,a6},{a3,a7}.
+// MMA 8c+2w+1 gets {a2,a6},{a3,a7}.  Positions past k are zero.
+template <int M>
 __device__ void build_fragments(const GemvParams& p, uint2* bfrag, float* rms) {
+  constexpr int BSTRIDE = 4 * M;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int M = p.m;
   // 1. inverse RMS per (row, segment)
   for (int job = warp; job < M * p.nseg; job += kWarps) {
     const int r = job / p.nseg, s = job % p.nseg;
@@ -199,12 +197,10 @@ __device__ void build_fragments(const GemvParams& p, uint2* bfrag, float* rms) {
   }
   __syncthreads();
   // 2. fragments
-  const int64_t kpad = (int64_t)p.nchunks * kChunk;
-  const int64_t groups = (int64_t)M * (kpad / 8);
-  const int bstride = 4 * M;
-  for (int64_t gi = tid; gi < groups; gi += kThreads) {
-    const int r = (int)(gi / (kpad / 8));
-    const int64_t kk = (gi % (kpad / 8)) * 8;
+  const int64_t gpr = (int64_t)p.nchunks * (kChunk / 8);  // 8-element groups per row
+  for (int64_t gi = tid; gi < (int64_t)M * gpr; gi += kThreads) {
+    const int r = (int)(gi / gpr);
+    const int64_t kk = (gi % gpr) * 8;
     uint32_t a[4] = {0u, 0u, 0u, 0u};  // bf16 pairs (a0,a1),(a2,a3),(a4,a5),(a6,a7)
     const int s = (p.nseg == 2 && kk >= p.kseg[0]) ? 1 : 0;
     const int64_t ko = kk - (s ? p.kseg[0] : 0);
@@ -226,97 +222,129 @@ __device__ void build_fragments(const GemvParams& p, uint2* bfrag, float* rms) {
     }
     const int c = (int)(kk / kChunk), t = (int)((kk % kChunk) / 32), w = (int)((kk % 32) / 8);
     const int L = 4 * r + t;
-    if (!NVFP4_GUARD((int64_t)(8 * c + 2 * w + 1) * bstride + L < (int64_t)p.nchunks * 8 * bstride &&
-                         L < bstride, 3, p.dev_status))
+    if (!NVFP4_GUARD((int64_t)(8 * c + 2 * w + 1) * BSTRIDE + L < (int64_t)p.nchunks * 8 * BSTRIDE &&
+                         L < BSTRIDE, 3, p.dev_status))
       continue;
     // element e of the group lives in half (e & 1) of a[e >> 1]
     const uint32_t e0 = a[0] & 0xFFFFu, e1 = a[0] >> 16, e2 = a[1] & 0xFFFFu, e3 = a[1] >> 16;
     const uint32_t e4 = a[2] & 0xFFFFu, e5 = a[2] >> 16, e6 = a[3] & 0xFFFFu, e7 = a[3] >> 16;
-    bfrag[(int64_t)(8 * c + 2 * w) * bstride + L] = make_uint2(e0 | (e4 << 16), e1 | (e5 << 16));
-    bfrag[(int64_t)(8 * c + 2 * w + 1) * bstride + L] = make_uint2(e2 | (e6 << 16), e3 | (e7 << 16));
+    bfrag[(int64_t)(8 * c + 2 * w) * BSTRIDE + L] = make_uint2(e0 | (e4 << 16), e1 | (e5 << 16));
+    bfrag[(int64_t)(8 * c + 2 * w + 1) * BSTRIDE + L] = make_uint2(e2 | (e6 << 16), e3 | (e7 << 16));
   }
 }
 
-// ------------------------------------------------------------------ kernel
-__global__ void __launch_bounds__(kThreads)
-gemv_kernel(const __grid_constant__ GemvParams p) {
-  extern __shared__ __align__(16) unsigned char smem[];
-  const int M = p.m;
-  const int bstride = 4 * M;
-  uint2* bfrag = reinterpret_cast<uint2*>(smem);
-  const size_t bbytes = (size_t)p.nchunks * 8 * bstride * sizeof(uint2);
-  float* red = reinterpret_cast<float*>(smem + bbytes);                // [kWarps][32][4]
-  float* rms = red + kWarps * 32 * 4;                                  // [16]
-  unsigned long long* kred = reinterpret_cast<unsigned long long*>(rms + 16);  // [kWarps][8]
+// Named barrier over the `count` threads of one tile group (ids 1..15).
+__device__ __forceinline__ void group_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
 
-  build_fragments(p, bfrag, rms);
-  __syncthreads();
+// ------------------------------------------------------------------ kernel
+// Work split: 16 warps per CTA; ks warps share one 16-row tile, each taking a
+// contiguous range of the k chunks (split K); a CTA takes 16/ks tiles at a
+// time and strides over the tiles persistently.  Each warp streams its
+// (tile, chunk) items in order with PF items in flight, across tile
+// boundaries; the full chunks need no predicates (rows past n are clamped to
+// a valid row whose results are dropped).  A chunk reaching past k (only when
+// k % 128 != 0) is loaded with predicates at the end of each tile.
+template <int M>
+__global__ void __launch_bounds__(kThreads, 2)
+gemv_kernel(const __grid_constant__ GemvParams p) {
+  constexpr int BSTRIDE = 4 * M;
+  extern __shared__ __align__(16) unsigned char smem[];
+  uint2* bfrag = reinterpret_cast<uint2*>(smem);
+  const size_t bbytes = (size_t)p.nchunks * 8 * BSTRIDE * sizeof(uint2);
+  float* red = reinterpret_cast<float*>(smem + bbytes);                // [2][kWarps][32][4]
+  float* rms = red + 2 * kWarps * 32 * 4;                              // [16]
+  unsigned long long* kred = reinterpret_cast<unsigned long long*>(rms + 16);  // [kWarps][32][2]
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, t = lane & 3;
   const int ks = p.ks;
   const int tpc = kWarps / ks;  // tiles per CTA iteration
   const int slot = warp / ks, kpart = warp % ks;
-  const int cpp = (p.nchunks + ks - 1) / ks;
-  const int c_begin = kpart * cpp;
-  const int c_end = min(p.nchunks, c_begin + cpp);
-  const bool bact = lane < bstride;
-  const float gs = __ldg(p.gscale) * 256.0f;  // g * 2^8 (the dequant fold)
+  // this warp's full chunks [cb, cb + L)
+  const int cb = (int)((int64_t)kpart * p.nfull / ks);
+  const int L = (int)((int64_t)(kpart + 1) * p.nfull / ks) - cb;
+  const bool tail = p.nfull < p.nchunks && kpart == ks - 1;
+  const int64_t ngroups = (p.ntiles + tpc - 1) / tpc;
+  const int n_iter = blockIdx.x < ngroups ? (int)((ngroups - 1 - blockIdx.x) / gridDim.x) + 1 : 0;
   const int64_t rowbytes = p.k / 2, rowscales = p.k / 16;
-  unsigned long long best[2] = {0ull, 0ull};
 
-  for (int64_t base = (int64_t)blockIdx.x * tpc; base < p.ntiles; base += (int64_t)gridDim.x * tpc) {
-    const int64_t tile = base + slot;
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    if (tile < p.ntiles && c_begin < c_end) {
-      const int64_t r0 = tile * 16 + g, r1 = r0 + 8;
-      const bool v0 = r0 < p.n, v1 = r1 < p.n;
-      const uint8_t* w0 = p.packed + (v0 ? r0 : 0) * rowbytes + 16 * t;
-      const uint8_t* w1 = p.packed + (v1 ? r1 : 0) * rowbytes + 16 * t;
-      const uint16_t* s0 = reinterpret_cast<const uint16_t*>(p.scales + (v0 ? r0 : 0) * rowscales) + t;
-      const uint16_t* s1 = reinterpret_cast<const uint16_t*>(p.scales + (v1 ? r1 : 0) * rowscales) + t;
-      uint4 qa[kPF], qb[kPF];
-      uint32_t sa[kPF], sb[kPF];
-      auto load = [&](int i, int c) {
-        bool kv = c < c_end && (int64_t)c * kChunk + 32 * t < p.k;
-        kv = kv && NVFP4_GUARD(!v0 || (r0 * rowbytes + 16 * t + (int64_t)c * 64 + 16 <= p.n * rowbytes &&
-                                       r0 * rowscales + 2 * t + 8 * (int64_t)c + 2 <= p.n * rowscales),
-                               4, p.dev_status);
-        kv = kv && NVFP4_GUARD(!v1 || (r1 * rowbytes + 16 * t + (int64_t)c * 64 + 16 <= p.n * rowbytes &&
-                                       r1 * rowscales + 2 * t + 8 * (int64_t)c + 2 <= p.n * rowscales),
-                               5, p.dev_status);
-        qa[i] = (kv && v0) ? ld_stream_u4(w0 + (int64_t)c * 64) : make_uint4(0, 0, 0, 0);
-        qb[i] = (kv && v1) ? ld_stream_u4(w1 + (int64_t)c * 64) : make_uint4(0, 0, 0, 0);
-        sa[i] = (kv && v0) ? (uint32_t)__ldg(s0 + 4 * c) : 0u;
-        sb[i] = (kv && v1) ? (uint32_t)__ldg(s1 + 4 * c) : 0u;
-      };
+  // load cursor: item (lt, lc) -> byte offsets of tile lt's two rows, chunk lc
+  // (32-bit offsets: the host rejects weights of 4 GiB or more)
+  int lt = 0, lc = 0;
+  uint32_t lo0 = 0, lo1 = 0;  // packed offsets of rows g, g + 8 at chunk cb
+  auto set_tile = [&](int it) {
+    const int64_t tile = ((int64_t)blockIdx.x + (int64_t)it * gridDim.x) * tpc + slot;
+    int64_t r0 = tile * 16 + g, r1 = r0 + 8;
+    r0 = r0 < p.n ? r0 : p.n - 1;
+    r1 = r1 < p.n ? r1 : p.n - 1;
+    lo0 = (uint32_t)(r0 * rowbytes + 16 * t + (int64_t)cb * 64);
+    lo1 = (uint32_t)(r1 * rowbytes + 16 * t + (int64_t)cb * 64);
+  };
+  const int total = n_iter * L;
+  uint4 qa[kPF], qb[kPF];
+  uint32_t sa[kPF], sb[kPF];
+  // The scale pair of a lane sits at byte (packed offset) / 8 of the scales:
+  // row r, chunk c, lane t -> packed byte r*k/2 + 64c + 16t, scale byte
+  // r*k/16 + 8c + 2t.
+  auto issue = [&](int i) {
+    if (lc == 0) set_tile(lt);
+    const uint32_t o0 = lo0 + (uint32_t)lc * 64, o1 = lo1 + (uint32_t)lc * 64;
+    qa[i] = ld_stream_u4(p.packed + o0);
+    qb[i] = ld_stream_u4(p.packed + o1);
+    sa[i] = __ldg(reinterpret_cast<const uint16_t*>(p.scales + (o0 >> 3)));
+    sb[i] = __ldg(reinterpret_cast<const uint16_t*>(p.scales + (o1 >> 3)));
+    if (++lc == L) { lc = 0; ++lt; }
+  };
+  // start streaming before the activation prologue
 #pragma unroll
-      for (int i = 0; i < kPF; ++i) load(i, c_begin + i);
-      for (int c = c_begin; c < c_end; c += kPF) {
-#pragma unroll
-        for (int i = 0; i < kPF; ++i) {
-          if (c + i < c_end) {
-            const int64_t boff = (int64_t)(8 * (c + i)) * bstride + lane;
-            chunk_mma(acc, qa[i], qb[i], sa[i], sb[i], bfrag + boff, bstride, bact,
-                      (int64_t)p.nchunks * 8 * bstride - boff, p.dev_status);
-            load(i, c + i + kPF);
-          }
-        }
+  for (int i = 0; i < kPF; ++i)
+    if (i < total) issue(i);
+
+  if (n_iter > 0 || blockIdx.x == 0) build_fragments<M>(p, bfrag, rms);
+  __syncthreads();
+
+  const float gs = __ldg(p.gscale) * 256.0f;  // g * 2^8 (the dequant fold)
+  const uint2* bbase = bfrag + (lane % BSTRIDE);
+  // running argmax keys of this lane's two batch columns live in shared memory
+  unsigned long long* best = kred + (warp * 32 + lane) * 2;
+  best[0] = 0ull;
+  best[1] = 0ull;
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  int ct = 0, cc = 0;  // compute cursor
+
+  auto epilogue = [&](int it) {
+    const int64_t tile = ((int64_t)blockIdx.x + (int64_t)it * gridDim.x) * tpc + slot;
+    if (tail) {  // the chunk reaching past k, with predicates
+      const int c = p.nfull;
+      const bool kv = (int64_t)c * kChunk + 32 * t < p.k;
+      int64_t r0 = tile * 16 + g, r1 = r0 + 8;
+      r0 = r0 < p.n ? r0 : p.n - 1;
+      r1 = r1 < p.n ? r1 : p.n - 1;
+      uint4 q0 = make_uint4(0, 0, 0, 0), q1 = make_uint4(0, 0, 0, 0);
+      uint32_t s0 = 0, s1 = 0;
+      if (kv && tile < p.ntiles) {
+        q0 = ld_stream_u4(p.packed + r0 * rowbytes + 16 * t + (int64_t)c * 64);
+        q1 = ld_stream_u4(p.packed + r1 * rowbytes + 16 * t + (int64_t)c * 64);
+        s0 = __ldg(reinterpret_cast<const uint16_t*>(p.scales + r0 * rowscales) + t + 4 * c);
+        s1 = __ldg(reinterpret_cast<const uint16_t*>(p.scales + r1 * rowscales) + t + 4 * c);
       }
+      chunk_mma<BSTRIDE>(acc, q0, q1, s0, s1, bbase + (int64_t)(8 * c) * BSTRIDE);
     }
     if (ks > 1) {
-      float* mine = red + (warp * 32 + lane) * 4;
+      float* rb = red + (size_t)(it & 1) * kWarps * 32 * 4;
       if (kpart != 0) {
+        float* mine = rb + (warp * 32 + lane) * 4;
         mine[0] = acc[0]; mine[1] = acc[1]; mine[2] = acc[2]; mine[3] = acc[3];
       }
-      __syncthreads();
+      group_sync(1 + slot, ks * 32);
       if (kpart == 0) {
         for (int j = 1; j < ks; ++j) {
-          const float* o = red + ((warp + j) * 32 + lane) * 4;
+          const float* o = rb + ((warp + j) * 32 + lane) * 4;
           acc[0] += o[0]; acc[1] += o[1]; acc[2] += o[2]; acc[3] += o[3];
         }
       }
-      __syncthreads();
     }
     if (kpart == 0 && tile < p.ntiles) {
       const int64_t rows[2] = {tile * 16 + g, tile * 16 + g + 8};
@@ -328,7 +356,8 @@ gemv_kernel(const __grid_constant__ GemvParams p) {
           const int mm = 2 * t + e;
           if (mm >= M) continue;
           const float v = acc[2 * h + e] * gs;
-          if (p.y != nullptr && NVFP4_GUARD(mm < M && rows[h] < p.n && rows[h] < p.ldy, 6, p.dev_status)) {
+          if (p.y != nullptr &&
+              NVFP4_GUARD(mm < M && rows[h] < p.n && rows[h] < p.ldy, 6, p.dev_status)) {
             if (p.y_dtype == NVFP4_DTYPE_F32)
               reinterpret_cast<float*>(p.y)[mm * p.ldy + rows[h]] = v;
             else
@@ -341,30 +370,42 @@ gemv_kernel(const __grid_constant__ GemvParams p) {
         }
       }
     }
+    acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+  };
+
+  if (L == 0) {
+    for (int it = 0; it < n_iter; ++it) epilogue(it);
+  } else {
+    for (int q = 0; q < total; q += kPF) {
+#pragma unroll
+      for (int i = 0; i < kPF; ++i) {
+        if (q + i < total) {
+          chunk_mma<BSTRIDE>(acc, qa[i], qb[i], sa[i], sb[i],
+                             bbase + (int64_t)(8 * (cb + cc)) * BSTRIDE);
+          if (q + i + kPF < total) issue(i);
+          if (++cc == L) {
+            epilogue(ct);
+            cc = 0;
+            ++ct;
+          }
+        }
+      }
+    }
   }
 
   if (p.keys == nullptr) return;
   // argmax: lanes sharing t hold the same two rows of the batch
-#pragma unroll
-  for (int e = 0; e < 2; ++e) {
-#pragma unroll
-    for (int o = 4; o < 32; o <<= 1) {
-      const unsigned long long other = __shfl_xor_sync(0xFFFFFFFFu, best[e], o);
-      best[e] = other > best[e] ? other : best[e];
-    }
-  }
-  if (g == 0) {
-    kred[warp * 8 + 2 * t] = best[0];
-    kred[warp * 8 + 2 * t + 1] = best[1];
-  }
   __syncthreads();
   if (threadIdx.x < (unsigned)M) {
+    // column m is held by the lanes with t = m / 2, slot m % 2, of every warp
+    const int m = threadIdx.x;
     unsigned long long b = 0ull;
-    for (int w = 0; w < kWarps; ++w) {
-      const unsigned long long o = kred[w * 8 + threadIdx.x];
-      b = o > b ? o : b;
-    }
-    if (b != 0ull) atomicMax(p.keys + threadIdx.x, b);
+    for (int w = 0; w < kWarps; ++w)
+      for (int gg = 0; gg < 8; ++gg) {
+        const unsigned long long o = kred[(w * 32 + gg * 4 + m / 2) * 2 + (m & 1)];
+        b = o > b ? o : b;
+      }
+    if (b != 0ull) atomicMax(p.keys + m, b);
   }
   __threadfence();
   __syncthreads();
@@ -379,6 +420,21 @@ gemv_kernel(const __grid_constant__ GemvParams p) {
           key == 0ull ? 0 : (int32_t)(0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFull));
     }
     if (threadIdx.x == 0) atomicExch(p.counter, 0u);
+  }
+}
+
+using KernelFn = void (*)(GemvParams);
+
+KernelFn kernel_for(int m) {
+  switch (m) {
+    case 1: return gemv_kernel<1>;
+    case 2: return gemv_kernel<2>;
+    case 3: return gemv_kernel<3>;
+    case 4: return gemv_kernel<4>;
+    case 5: return gemv_kernel<5>;
+    case 6: return gemv_kernel<6>;
+    case 7: return gemv_kernel<7>;
+    default: return gemv_kernel<8>;
   }
 }
 
@@ -413,22 +469,25 @@ int launch_gemv(const w4a16_act_segment* seg, int nseg, int m, const nvfp4_weigh
   p.dev_status = dev_status;
   p.ntiles = nvfp4::cdiv(w->n, 16);
   p.nchunks = (int)nvfp4::cdiv(w->k, kChunk);
+  p.nfull = (int)(w->k / kChunk);
 
   const size_t bbytes = (size_t)p.nchunks * 8 * 4 * m * sizeof(uint2);
-  const size_t smem = bbytes + kWarps * 32 * 4 * sizeof(float) + 16 * sizeof(float) +
-                      kWarps * 8 * sizeof(unsigned long long);
-  const int occ = nvfp4::occupancy(reinterpret_cast<const void*>(gemv_kernel), kThreads, smem);
+  const size_t smem = bbytes + 2 * kWarps * 32 * 4 * sizeof(float) + 16 * sizeof(float) +
+                      kWarps * 32 * 2 * sizeof(unsigned long long);
+  KernelFn fn = kernel_for(m);
+  const int occ = nvfp4::occupancy(reinterpret_cast<const void*>(fn), kThreads, smem);
   if (occ < 1) return NVFP4_ERR_CUDA;
   const int sms = nvfp4::sm_count();
-  const int64_t slots = (int64_t)sms * occ * kWarps;  // resident warps
-  // split K until every resident warp has work, keeping >= 2 chunks per part
+  const int64_t slots = (int64_t)sms * occ;  // resident CTAs
+  // Split K (ks warps per tile) until the resident CTAs each get several tile
+  // groups to stream, keeping at least 4 full chunks per warp.
   int ks = 1;
-  while (ks < kWarps && p.ntiles * ks < slots && p.nchunks / (2 * ks) >= 2) ks *= 2;
+  while (ks < kWarps && nvfp4::cdiv(p.ntiles, kWarps / ks) < 4 * slots && p.nfull / (2 * ks) >= 4)
+    ks *= 2;
   p.ks = ks;
-  const int tpc = kWarps / ks;
-  int64_t grid = nvfp4::cdiv(p.ntiles, tpc);
-  if (grid > (int64_t)sms * occ) grid = (int64_t)sms * occ;
-  gemv_kernel<<<(unsigned)grid, kThreads, smem, stream>>>(p);
+  const int64_t ngroups = nvfp4::cdiv(p.ntiles, kWarps / ks);
+  const int64_t grid = ngroups < slots ? ngroups : slots;
+  fn<<<(unsigned)grid, kThreads, smem, stream>>>(p);
   if (cudaGetLastError() != cudaSuccess) return NVFP4_ERR_CUDA;
   return NVFP4_OK;
 }
