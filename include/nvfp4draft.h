@@ -155,6 +155,29 @@ int w4a16_gemv_argmax(const w4a16_act_segment *seg, int nseg, int m,
                       int32_t *argmax, const nvfp4_exec *ex);
 
 /*
+ * w4a16_gemv_argmax_noalloc -- w4a16_gemv_argmax for callers that cannot
+ * allocate device memory.  The pages have no counterpart of this call.
+ * Some callers cannot call cudaMalloc at call time: a serving loop running
+ * under a fixed device-memory budget handed out up front, a host framework
+ * whose allocator forbids side allocations, or code that must not hit the
+ * implicit device synchronisation of cudaMalloc/cudaFree in the decode path.
+ * This variant takes no workspace: its argmax scratch (W4A16_GEMV_MAX_M keys
+ * and a counter) is a fixed 256-byte __device__ array inside the library,
+ * which every GPU that loads the library keeps until the process exits.
+ *   Arguments as w4a16_gemv_argmax, except: no nvfp4_exec; stream is a
+ *   cudaStream_t (NULL = legacy default stream); dev_status is nullable.
+ *   m > W4A16_GEMV_MAX_M (beyond the scratch) -> NVFP4_ERR_SHAPE.
+ * The first call on a device looks up the array's device address (with that
+ * device current); make that first call before any stream capture.  Each call
+ * clears the scratch on its stream first.  All calls share the array, so
+ * calls that overlap on the GPU (other streams, other host threads) race.
+ * Allocates nothing: no cudaMalloc, cudaFree or allocating library routine.
+ */
+int w4a16_gemv_argmax_noalloc(const w4a16_act_segment *seg, int nseg, int m,
+                              const nvfp4_weight *w, float *logits, int64_t ld_logits,
+                              int32_t *argmax, void *stream, int32_t *dev_status);
+
+/*
  * w4a16_gemm -- prefill W4A16 GEMM, C[m, n] = bf16( g * A[m, :] . w~[n, :] ),
  * w~ dequantised exactly to BF16 and multiplied with BF16 tensor-core MMAs
  * accumulating in FP32, in 128-row tiles of A.  This is the lossless

@@ -75,7 +75,9 @@ def load(path: str = LIB_PATH):
     L.w4a16_gemv.argtypes = [P(_Segment), i32, i32, P(_Weight), vp, i32, i64, P(_Exec)]
     L.w4a16_gemv_argmax.argtypes = [P(_Segment), i32, i32, P(_Weight), vp, i64, vp, P(_Exec)]
     L.w4a16_gemm.argtypes = [vp, i64, i64, P(_Weight), vp, i64, P(_Exec)]
-    for f in EXPORTED:
+    L.w4a16_gemv_argmax_noalloc.argtypes = [P(_Segment), i32, i32, P(_Weight), vp, i64, vp, vp,
+                                            vp]
+    for f in EXPORTED + ("w4a16_gemv_argmax_noalloc",):
         getattr(L, f).restype = ctypes.c_int
     _LIB = L
     return L
@@ -201,6 +203,30 @@ def w4a16_gemv_argmax(segments: Sequence, weight: Nvfp4Weight, logits: bool = Tr
                                   out_logits.stride(0) if out_logits is not None else 0,
                                   out_argmax.data_ptr(), ctypes.byref(ex))
     _check("w4a16_gemv_argmax", rc)
+    return out_logits, out_argmax
+
+
+def w4a16_gemv_argmax_noalloc(segments: Sequence, weight: Nvfp4Weight,
+                              out_logits: Optional[torch.Tensor] = None,
+                              out_argmax: Optional[torch.Tensor] = None, logits: bool = True,
+                              stream=None, dev_status: Optional[torch.Tensor] = None):
+    """w4a16_gemv_argmax without a workspace: the library's own fixed device
+    scratch holds the argmax keys (for callers that cannot allocate).  Calls
+    that overlap on the GPU share that scratch and race.  Output tensors are
+    allocated here only when not passed in."""
+    segs, m = _segments(segments)
+    dev = weight.packed.device
+    if logits and out_logits is None:
+        out_logits = torch.empty((m, weight.n), dtype=torch.float32, device=dev)
+    if out_argmax is None:
+        out_argmax = torch.empty(m, dtype=torch.int32, device=dev)
+    w = weight.c()
+    rc = load().w4a16_gemv_argmax_noalloc(
+        segs, len(segments), m, ctypes.byref(w),
+        out_logits.data_ptr() if out_logits is not None else None,
+        out_logits.stride(0) if out_logits is not None else 0, out_argmax.data_ptr(),
+        _stream(stream), dev_status.data_ptr() if dev_status is not None else None)
+    _check("w4a16_gemv_argmax_noalloc", rc)
     return out_logits, out_argmax
 
 

@@ -57,9 +57,7 @@ int occupancy(const void* func, int threads, size_t smem) {
 
 }  // namespace nvfp4
 
-namespace {
-
-using nvfp4::aligned16;
+namespace nvfp4 {
 
 int check_weight(const nvfp4_weight* w) {
   if (w == nullptr || w->packed == nullptr || w->scales == nullptr || w->global_scale == nullptr)
@@ -90,6 +88,14 @@ int check_segments(const w4a16_act_segment* seg, int nseg, int m, int64_t k) {
   if (total != k) return NVFP4_ERR_SHAPE;
   return NVFP4_OK;
 }
+
+}  // namespace nvfp4
+
+namespace {
+
+using nvfp4::aligned16;
+using nvfp4::check_segments;
+using nvfp4::check_weight;
 
 cudaStream_t stream_of(const nvfp4_exec* ex) {
   return ex ? reinterpret_cast<cudaStream_t>(ex->stream) : nullptr;

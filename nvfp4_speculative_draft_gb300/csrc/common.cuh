@@ -43,6 +43,11 @@ int sm_count();
 // is being captured into a CUDA graph issue no CUDA API calls here.
 int occupancy(const void* func, int threads, size_t smem);
 
+// Host-side argument checks shared by the entry points (status codes of
+// nvfp4draft.h).
+int check_weight(const nvfp4_weight* w);
+int check_segments(const w4a16_act_segment* seg, int nseg, int m, int64_t k);
+
 }  // namespace nvfp4
 
 // Launchers implemented in the kernel translation units.
