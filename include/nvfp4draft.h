@@ -187,7 +187,9 @@ int w4a16_gemv_argmax_noalloc(const w4a16_act_segment *seg, int nseg, int m,
  *   a_bf16   device BF16 [m, lda], 16-byte aligned, lda % 8 == 0, lda >= k.
  *   m >= 1 (any; the last tile is masked); w->n % 128 == 0; w->k % 64 == 0.
  *   c_bf16   device BF16 [m, ldc], 16-byte aligned, ldc % 8 == 0, ldc >= n.
- * Workspace: none.
+ *   w->scales 4-byte aligned.
+ * Workspace: none.  Waits inside the kernel are bounded; one that runs out
+ * writes NVFP4_ERR_TIMEOUT to ex->dev_status and leaves C incomplete.
  */
 int w4a16_gemm(const void *a_bf16, int64_t m, int64_t lda, const nvfp4_weight *w,
                void *c_bf16, int64_t ldc, const nvfp4_exec *ex);

@@ -167,7 +167,8 @@ int w4a16_gemm(const void* a_bf16, int64_t m, int64_t lda, const nvfp4_weight* w
   if (a_bf16 == nullptr || c_bf16 == nullptr) return NVFP4_ERR_NULL;
   if (m < 1 || w->n % 128 != 0 || w->k % 64 != 0 || lda < w->k || ldc < w->n)
     return NVFP4_ERR_SHAPE;
-  if (!aligned16(a_bf16) || !aligned16(c_bf16) || lda % 8 != 0 || ldc % 8 != 0)
+  if (!aligned16(a_bf16) || !aligned16(c_bf16) || lda % 8 != 0 || ldc % 8 != 0 ||
+      (reinterpret_cast<uintptr_t>(w->scales) & 3u))
     return NVFP4_ERR_ALIGN;
   return launch_gemm(a_bf16, m, lda, w, c_bf16, ldc, status_of(ex), stream_of(ex));
 }

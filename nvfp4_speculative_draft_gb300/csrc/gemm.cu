@@ -1,82 +1,407 @@
-// gemm.cu -- prefill W4A16 GEMM, C = bf16(g * A . w~^T), w~ = e4m3(s) * e2m1(c).
+// gemm.cu -- prefill W4A16 GEMM on the 5th-generation tensor cores (sm_103a).
 //
-// First correct version on CUDA cores (64x64 output tiles, FP32 FMA over the
-// exactly dequantised weights); the tensor-core (tcgen05/TMEM) kernel replaces
-// it.  Numerics follow the lossless FP4->BF16 dequant + BF16 product of the
-// M=128 prefill dispatch in "spark_model/layers/qwen3_attention/prefill_weights.rs".
+//   C[m, n] = bf16( g * sum_k A[m, k] * w~[n, k] ),   w~ = e4m3(s[n, k/16]) * e2m1(c[n, k])
+//
+// Numerics of the lossless prefill path of "spark_model/layers/qwen3_attention/
+// prefill_weights.rs" (w4a16_gemm_m128_dispatch, BF16 tensor-core variant): the
+// FP4 weight is dequantised exactly to BF16 and multiplied with BF16 MMAs
+// accumulating in FP32, one 128-row tile of A at a time.
+//
+// One CTA computes a 128 x 256 output tile (M = 128 activation rows, N = 256
+// weight rows) with tcgen05.mma (cta_group::1, kind::f16, BF16 x BF16 -> FP32),
+// the accumulator in tensor memory (256 TMEM columns).  K runs in steps of 64
+// through a 4-stage shared-memory ring:
+//   warp 0      TMA producer: the 128 x 64 BF16 A tile by cp.async.bulk.tensor
+//               (128-byte swizzle; rows past m read as zero);
+//   warp 1      allocates TMEM, issues the 4 MMAs (K = 16 each) of a stage from
+//               one thread, commits each stage's completion to its "empty"
+//               barrier and the last one to the accumulator barrier;
+//   warps 2..9  dequantise the 256 x 64 weight tile (one row per thread: 32
+//               bytes of codes + 4 scale bytes, prefetched one step ahead) into
+//               the same 128-byte-swizzled K-major layout, fence the async proxy
+//               and arrive on the stage's "full" barrier; after the K loop they
+//               are the epilogue: tcgen05.ld of their TMEM lane quadrant, times
+//               g, round to BF16, store.
+// Dequantisation: E2M1 nibble pairs become BF16 bit patterns of value * 2^-126
+// (integer ops), then one packed BF16 multiply by the block scale * 2^118
+// (exact); the 2^8 left over is folded into g in the epilogue.
+// Every wait is bounded (2 s of globaltimer): a wait that runs out records
+// NVFP4_ERR_TIMEOUT in the caller's status word and the CTA unwinds, freeing
+// its TMEM.
+#include <cuda.h>
 #include <cuda_fp8.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
 
 #include "common.cuh"
 
 namespace {
 
-constexpr int BM = 64, BN = 64, BK = 32;
+constexpr int BM = 128, BN = 256, BK = 64;
+constexpr int kStages = 4;
+constexpr int kABytes = BM * BK * 2;  // 16 KB
+constexpr int kBBytes = BN * BK * 2;  // 32 KB
+constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kDequantWarps = 8;
+constexpr int kThreads = (2 + kDequantWarps) * 32;
+constexpr int kTmemCols = 256;
+constexpr size_t kSmemBytes = 1024 /*alignment slack*/ + (size_t)kStages * kStageBytes + 256;
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
-__device__ __forceinline__ float e2m1_val(uint32_t c) {
-  const float mag[8] = {0.f, 0.5f, 1.f, 1.5f, 2.f, 3.f, 4.f, 6.f};
-  const float v = mag[c & 7];
-  return (c & 8) ? -v : v;
+// ------------------------------------------------------------ PTX helpers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ unsigned long long globaltimer() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait: false if it gave up (timeout here, or another role aborted).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile uint32_t* abort,
+                                          int32_t* dev_status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
+    if (globaltimer() - t0 > kWaitLimitNs) {
+      *abort = 1u;
+      nvfp4::report(dev_status, NVFP4_ERR_TIMEOUT);
+      return false;
+    }
+  }
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
+// 1024 bytes apart (SBO), version 1 (bits 46..47), start address >> 4.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr) {
+  return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+// Instruction descriptor, kind::f16: D = F32 (bits 4..5 = 1), A = B = BF16
+// (bits 7..9 = 1, 10..12 = 1), both K-major, N >> 3 at bits 17..22, M >> 4 at
+// bits 24..28.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
+                            ((uint32_t)(BM >> 4) << 24);
+
+__device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+        "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]),
+        "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]),
+        "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-__global__ void __launch_bounds__(256)
-gemm_simt_kernel(const __nv_bfloat16* __restrict__ A, int64_t M, int64_t lda,
-                 const uint8_t* __restrict__ packed, const uint8_t* __restrict__ scales,
-                 const float* __restrict__ gscale, int64_t N, int64_t K,
-                 __nv_bfloat16* __restrict__ C, int64_t ldc) {
-  __shared__ float As[BK][BM + 4];
-  __shared__ float Bs[BK][BN + 4];
-  const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
+__device__ __forceinline__ uint4 ld_nc_u4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+// Two E4M3 scales (low byte first) -> bf16x2 patterns of scale * 2^118, each
+// replicated into both halves (see the GEMV for the construction).
+__device__ __forceinline__ void decode_scales(uint32_t s2, uint32_t& lo, uint32_t& hi) {
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)s2, __NV_E4M3);
+  uint32_t v = ((uint32_t)h.x | ((uint32_t)h.y << 16)) >> 3;
+  v = bf16x2_mul(v, 0x79007900u);
+  v = bf16x2_mul(v, 0x79007900u);
+  lo = __byte_perm(v, 0, 0x1010);
+  hi = __byte_perm(v, 0, 0x3232);
+}
+// prmt.b32 in its generic mode: a selector nibble with bit 3 set replicates
+// the sign bit of the selected byte (CUDA's __byte_perm masks that bit off).
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+// The 8 E2M1 codes of word q (k = 8w..8w+7, natural order) -> 4 bf16x2 patterns
+// (value * 2^-126) times scale pattern s.  Pair p = (nibble 2p, nibble 2p+1):
+// one byte_perm places nibble 2p in bits 0..3 and nibble 2p+1 in bits 16..19
+// (zero bytes come from the sign-replicate mode on bytes whose top bit is 0);
+// the multiply by 0x1040 makes the two shifted copies whose masked bits are
+// the sign (bit 15) and the 3 magnitude bits (8..6) of each half.
+__device__ __forceinline__ uint4 dequant_word(uint32_t q, uint32_t s) {
+  const uint32_t ev = q & 0x0F0F0F0Fu, od = (q >> 4) & 0x0F0F0F0Fu;
+  const uint32_t p0 = prmt(ev, od, 0xC480u);
+  const uint32_t p1 = prmt(ev, od, 0xD591u);
+  const uint32_t p2 = prmt(ev, od, 0xE6A2u);
+  const uint32_t p3 = prmt(ev, od, 0xF7B3u);
+  uint4 r;
+  r.x = bf16x2_mul((p0 * 0x1040u) & 0x81C081C0u, s);
+  r.y = bf16x2_mul((p1 * 0x1040u) & 0x81C081C0u, s);
+  r.z = bf16x2_mul((p2 * 0x1040u) & 0x81C081C0u, s);
+  r.w = bf16x2_mul((p3 * 0x1040u) & 0x81C081C0u, s);
+  return r;
+}
+
+struct GemmParams {
+  const uint8_t* packed;
+  const uint8_t* scales;
+  const float* gscale;
+  __nv_bfloat16* c;
+  int64_t m, n, k, ldc;
+  int32_t* dev_status;
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ GemmParams p) {
+  extern __shared__ unsigned char smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;  // 128-byte swizzle wants 1 KB alignment
+  unsigned char* const smem = smem_raw + (base - raw);
+  const uint32_t bars = base + kStages * kStageBytes;
+  auto full_a = [&](int s) { return bars + 8u * s; };
+  auto full_b = [&](int s) { return bars + 8u * (kStages + s); };
+  auto empty = [&](int s) { return bars + 8u * (2 * kStages + s); };
+  const uint32_t accum_bar = bars + 8u * (3 * kStages);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kStages * kStageBytes + 8 * (3 * kStages + 1));
+  volatile uint32_t* abort = tmem_slot + 1;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t m0 = (int64_t)blockIdx.y * BM, n0 = (int64_t)blockIdx.x * BN;
-  float acc[4][4] = {};
-  for (int64_t k0 = 0; k0 < K; k0 += BK) {
-    for (int e = threadIdx.x; e < BM * BK; e += 256) {
-      const int r = e / BK, kk = e % BK;
-      const int64_t gm = m0 + r;
-      As[kk][r] = gm < M ? __bfloat162float(A[gm * lda + k0 + kk]) : 0.f;
+  const int nk = (int)(p.k / BK);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(full_a(s), 1);
+      mbar_init(full_b(s), kDequantWarps);
+      mbar_init(empty(s), 1);
     }
-    for (int e = threadIdx.x; e < BN * BK; e += 256) {
-      const int r = e / BK, kk = e % BK;
-      const int64_t gn = n0 + r, gk = k0 + kk;
-      const uint32_t byte = packed[gn * (K / 2) + gk / 2];
-      const uint32_t code = (gk & 1) ? (byte >> 4) : (byte & 15u);
-      const __half_raw sh =
-          __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)scales[gn * (K / 16) + gk / 16], __NV_E4M3);
-      Bs[kk][r] = e2m1_val(code) * __half2float(__half(sh));
-    }
-    __syncthreads();
-#pragma unroll 8
-    for (int kk = 0; kk < BK; ++kk) {
-      float a[4], b[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) a[i] = As[kk][ty * 4 + i];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) b[j] = Bs[kk][tx * 4 + j];
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
-    }
-    __syncthreads();
+    mbar_init(accum_bar, 1);
+    *abort = 0u;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  const float g = *gscale;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int64_t gm = m0 + ty * 4 + i;
-    if (gm >= M) continue;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) C[gm * ldc + n0 + tx * 4 + j] = __float2bfloat16_rn(acc[i][j] * g);
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      for (int kb = 0; kb < nk; ++kb) {
+        const int s = kb % kStages, r = kb / kStages;
+        if (r > 0 && !mbar_wait(empty(s), (r - 1) & 1, abort, p.dev_status)) break;
+        mbar_arrive_expect_tx(full_a(s), kABytes);
+        tma_load_2d(base + s * kStageBytes, &tmap_a, kb * BK, (int)m0, full_a(s));
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      bool ok = true;
+      for (int kb = 0; kb < nk && ok; ++kb) {
+        const int s = kb % kStages, r = kb / kStages;
+        ok = mbar_wait(full_a(s), r & 1, abort, p.dev_status) &&
+             mbar_wait(full_b(s), r & 1, abort, p.dev_status);
+        if (!ok) break;
+        tc_fence_after();
+        const uint64_t ad = smem_desc(base + s * kStageBytes);
+        const uint64_t bd = smem_desc(base + s * kStageBytes + kABytes);
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk)  // advance 32 bytes (16 BF16) along K
+          mma_bf16(tmem, ad + 2 * kk, bd + 2 * kk, (kb > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(empty(s));
+      }
+      mma_commit(accum_bar);  // fires once every issued MMA has completed
+    }
+  } else {
+    // ------------------------------------------------ dequant, then epilogue
+    const int r = threadIdx.x - 64;  // B-tile row 0..255
+    const int64_t nrow = n0 + r;
+    const bool valid = nrow < p.n;
+    const uint8_t* wrow = p.packed + (valid ? nrow : 0) * (p.k / 2);
+    const uint32_t* srow = reinterpret_cast<const uint32_t*>(p.scales + (valid ? nrow : 0) * (p.k / 16));
+    uint4 q0 = make_uint4(0, 0, 0, 0), q1 = make_uint4(0, 0, 0, 0);
+    uint32_t sc = 0;
+    if (valid && nk > 0) {
+      q0 = ld_nc_u4(wrow);
+      q1 = ld_nc_u4(wrow + 16);
+      sc = __ldg(srow);
+    }
+    const uint32_t swz = (uint32_t)(r & 7);
+    bool ok = true;
+    for (int kb = 0; kb < nk; ++kb) {
+      const int s = kb % kStages, rr = kb / kStages;
+      const uint4 c0 = q0, c1 = q1;
+      const uint32_t cs = sc;
+      if (valid && kb + 1 < nk) {  // prefetch the next step's row slice
+        q0 = ld_nc_u4(wrow + (int64_t)(kb + 1) * 32);
+        q1 = ld_nc_u4(wrow + (int64_t)(kb + 1) * 32 + 16);
+        sc = __ldg(srow + kb + 1);
+      }
+      if (rr > 0 && !mbar_wait(empty(s), (rr - 1) & 1, abort, p.dev_status)) {
+        ok = false;
+        break;
+      }
+      uint32_t S[4];
+      decode_scales(cs & 0xFFFFu, S[0], S[1]);
+      decode_scales(cs >> 16, S[2], S[3]);
+      const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+      unsigned char* brow = smem + s * kStageBytes + kABytes + r * 128;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {  // 16-byte chunk j holds k = 8j .. 8j+7
+        const uint4 v = dequant_word(words[j], S[j >> 1]);
+        *reinterpret_cast<uint4*>(brow + ((j ^ swz) << 4)) = v;
+      }
+      fence_proxy_async();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(full_b(s));
+    }
+    // epilogue: warp quadrant q owns TMEM lanes 32q..32q+31 (rows of the tile)
+    __syncwarp();
+    if (ok && mbar_wait(accum_bar, 0, abort, p.dev_status)) {
+      __syncwarp();
+      tc_fence_after();
+      const int q = warp & 3, h = (warp - 2) >> 2;
+      const int64_t row = m0 + 32 * q + lane;
+      const float gs = __ldg(p.gscale) * 256.0f;
+#pragma unroll 1
+      for (int j = 0; j < 4; ++j) {
+        const int col = 128 * h + 32 * j;
+        uint32_t v[32];
+        tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)col, v);
+        if (row < p.m && n0 + col < p.n) {
+          uint32_t packed16[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(v[2 * i]) * gs,
+                                                      __uint_as_float(v[2 * i + 1]) * gs);
+            packed16[i] = *reinterpret_cast<uint32_t*>(&b2);
+          }
+          uint4* dst = reinterpret_cast<uint4*>(p.c + row * p.ldc + n0 + col);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            dst[i] = make_uint4(packed16[4 * i], packed16[4 * i + 1], packed16[4 * i + 2],
+                                packed16[4 * i + 3]);
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
+                 : "memory");
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static std::mutex mu;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (fn == nullptr) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
 }
 
 }  // namespace
 
 int launch_gemm(const void* a, int64_t m, int64_t lda, const nvfp4_weight* w, void* c,
                 int64_t ldc, int32_t* dev_status, cudaStream_t stream) {
-  (void)dev_status;
-  dim3 grid((unsigned)(w->n / BN), (unsigned)nvfp4::cdiv(m, BM));
-  gemm_simt_kernel<<<grid, 256, 0, stream>>>(reinterpret_cast<const __nv_bfloat16*>(a), m, lda,
-                                             w->packed, w->scales, w->global_scale, w->n, w->k,
-                                             reinterpret_cast<__nv_bfloat16*>(c), ldc);
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+  if (enc == nullptr) return NVFP4_ERR_CUDA;
+  CUtensorMap tmap;
+  const cuuint64_t dims[2] = {(cuuint64_t)w->k, (cuuint64_t)m};
+  const cuuint64_t strides[1] = {(cuuint64_t)lda * 2};
+  const cuuint32_t box[2] = {BK, BM};
+  const cuuint32_t estr[2] = {1, 1};
+  if (enc(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(a), dims, strides, box, estr,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return NVFP4_ERR_CUDA;
+  GemmParams p;
+  p.packed = w->packed;
+  p.scales = w->scales;
+  p.gscale = w->global_scale;
+  p.c = reinterpret_cast<__nv_bfloat16*>(c);
+  p.m = m;
+  p.n = w->n;
+  p.k = w->k;
+  p.ldc = ldc;
+  p.dev_status = dev_status;
+  if (nvfp4::occupancy(reinterpret_cast<const void*>(gemm_tcgen05_kernel), kThreads, kSmemBytes) < 1)
+    return NVFP4_ERR_CUDA;
+  dim3 grid((unsigned)nvfp4::cdiv(w->n, BN), (unsigned)nvfp4::cdiv(m, BM));
+  gemm_tcgen05_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tmap, p);
   if (cudaGetLastError() != cudaSuccess) return NVFP4_ERR_CUDA;
   return NVFP4_OK;
 }
