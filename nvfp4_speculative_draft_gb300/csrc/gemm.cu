@@ -44,8 +44,10 @@ constexpr int kABytes = BM * BK * 2;  // 16 KB
 constexpr int kBBytes = BN * BK * 2;  // 32 KB
 constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kDequantWarps = 8;
-constexpr int kThreads = (2 + kDequantWarps) * 32;
-constexpr int kTmemCols = 256;
+constexpr int kEpilogueWarps = 4;
+constexpr int kThreads = (2 + kDequantWarps + kEpilogueWarps) * 32;
+constexpr int kTmemCols = 2 * BN;  // two accumulators: epilogue of one tile overlaps the next
+constexpr int kPrefetch = 3;       // k steps of weight rows in flight per dequant thread
 constexpr size_t kSmemBytes = 1024 /*alignment slack*/ + (size_t)kStages * kStageBytes + 256;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
@@ -203,8 +205,16 @@ struct GemmParams {
   const float* gscale;
   __nv_bfloat16* c;
   int64_t m, n, k, ldc;
+  int mtiles, ntiles;
   int32_t* dev_status;
 };
+
+// Tile t of the persistent schedule: consecutive t share one 256-row weight
+// slice (n tile), so the CTAs working on it at the same time find it in L2.
+__device__ __forceinline__ void tile_coords(const GemmParams& p, int t, int64_t& m0, int64_t& n0) {
+  m0 = (int64_t)(t % p.mtiles) * BM;
+  n0 = (int64_t)(t / p.mtiles) * BN;
+}
 
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ GemmParams p) {
@@ -216,13 +226,19 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
   auto full_a = [&](int s) { return bars + 8u * s; };
   auto full_b = [&](int s) { return bars + 8u * (kStages + s); };
   auto empty = [&](int s) { return bars + 8u * (2 * kStages + s); };
-  const uint32_t accum_bar = bars + 8u * (3 * kStages);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kStages * kStageBytes + 8 * (3 * kStages + 1));
+  auto tmem_full = [&](int b) { return bars + 8u * (3 * kStages + b); };
+  auto tmem_empty = [&](int b) { return bars + 8u * (3 * kStages + 2 + b); };
+  uint32_t* tmem_slot =
+      reinterpret_cast<uint32_t*>(smem + kStages * kStageBytes + 8 * (3 * kStages + 4));
   volatile uint32_t* abort = tmem_slot + 1;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t m0 = (int64_t)blockIdx.y * BM, n0 = (int64_t)blockIdx.x * BN;
   const int nk = (int)(p.k / BK);
+  const int ntiles_all = p.mtiles * p.ntiles;
+  // tiles of this CTA: blockIdx.x, blockIdx.x + gridDim.x, ...
+  const int my_tiles =
+      (int)blockIdx.x < ntiles_all ? (ntiles_all - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+  const int total = my_tiles * nk;  // k steps streamed through the ring
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -230,7 +246,10 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
       mbar_init(full_b(s), kDequantWarps);
       mbar_init(empty(s), 1);
     }
-    mbar_init(accum_bar, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tmem_full(b), 1);
+      mbar_init(tmem_empty(b), kEpilogueWarps);
+    }
     *abort = 0u;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -249,8 +268,11 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
   if (warp == 0) {
     // ---------------------------------------------------------- TMA producer
     if (lane == 0) {
-      for (int kb = 0; kb < nk; ++kb) {
-        const int s = kb % kStages, r = kb / kStages;
+      for (int g = 0; g < total; ++g) {
+        const int s = g % kStages, r = g / kStages;
+        const int kb = g % nk;
+        int64_t m0, n0;
+        tile_coords(p, (int)blockIdx.x + (g / nk) * (int)gridDim.x, m0, n0);
         if (r > 0 && !mbar_wait(empty(s), (r - 1) & 1, abort, p.dev_status)) break;
         mbar_arrive_expect_tx(full_a(s), kABytes);
         tma_load_2d(base + s * kStageBytes, &tmap_a, kb * BK, (int)m0, full_a(s));
@@ -260,77 +282,105 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       bool ok = true;
-      for (int kb = 0; kb < nk && ok; ++kb) {
-        const int s = kb % kStages, r = kb / kStages;
-        ok = mbar_wait(full_a(s), r & 1, abort, p.dev_status) &&
-             mbar_wait(full_b(s), r & 1, abort, p.dev_status);
-        if (!ok) break;
+      for (int it = 0; it < my_tiles && ok; ++it) {
+        const int ab = it & 1;
+        if (it >= 2 && !mbar_wait(tmem_empty(ab), ((it >> 1) - 1) & 1, abort, p.dev_status)) break;
         tc_fence_after();
-        const uint64_t ad = smem_desc(base + s * kStageBytes);
-        const uint64_t bd = smem_desc(base + s * kStageBytes + kABytes);
+        const uint32_t d = tmem + (uint32_t)(ab * BN);
+        for (int kb = 0; kb < nk; ++kb) {
+          const int g = it * nk + kb;
+          const int s = g % kStages, r = g / kStages;
+          ok = mbar_wait(full_a(s), r & 1, abort, p.dev_status) &&
+               mbar_wait(full_b(s), r & 1, abort, p.dev_status);
+          if (!ok) break;
+          tc_fence_after();
+          const uint64_t ad = smem_desc(base + s * kStageBytes);
+          const uint64_t bd = smem_desc(base + s * kStageBytes + kABytes);
 #pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk)  // advance 32 bytes (16 BF16) along K
-          mma_bf16(tmem, ad + 2 * kk, bd + 2 * kk, (kb > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(empty(s));
+          for (int kk = 0; kk < BK / 16; ++kk)  // advance 32 bytes (16 BF16) along K
+            mma_bf16(d, ad + 2 * kk, bd + 2 * kk, (kb > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(empty(s));
+        }
+        mma_commit(tmem_full(ab));  // fires once the tile's MMAs have completed
       }
-      mma_commit(accum_bar);  // fires once every issued MMA has completed
+    }
+  } else if (warp < 2 + kDequantWarps) {
+    // --------------------------------------------------------------- dequant
+    const int r = threadIdx.x - 64;  // B-tile row 0..255
+    const uint32_t swz = (uint32_t)(r & 7);
+    uint4 qa[kPrefetch], qb[kPrefetch];
+    uint32_t qs[kPrefetch];
+    // load cursor over (tile, k step)
+    int lg = 0;
+    auto issue = [&](int i) {
+      const int it = lg / nk, kb = lg - it * nk;
+      int64_t m0, n0;
+      tile_coords(p, (int)blockIdx.x + it * (int)gridDim.x, m0, n0);
+      const int64_t nrow = n0 + r;
+      if (nrow < p.n) {
+        const uint8_t* w = p.packed + nrow * (p.k / 2) + (int64_t)kb * 32;
+        qa[i] = ld_nc_u4(w);
+        qb[i] = ld_nc_u4(w + 16);
+        qs[i] = __ldg(reinterpret_cast<const uint32_t*>(p.scales + nrow * (p.k / 16)) + kb);
+      } else {  // rows past n: zero weights (their outputs are not stored)
+        qa[i] = make_uint4(0, 0, 0, 0);
+        qb[i] = make_uint4(0, 0, 0, 0);
+        qs[i] = 0u;
+      }
+      ++lg;
+    };
+#pragma unroll
+    for (int i = 0; i < kPrefetch; ++i)
+      if (i < total) issue(i);
+    bool ok = true;
+    for (int g0 = 0; g0 < total && ok; g0 += kPrefetch) {
+#pragma unroll
+      for (int i = 0; i < kPrefetch; ++i) {
+        const int g = g0 + i;
+        if (g < total && ok) {
+          const int s = g % kStages, rr = g / kStages;
+          const uint4 c0 = qa[i], c1 = qb[i];
+          const uint32_t cs = qs[i];
+          if (g + kPrefetch < total) issue(i);
+          if (rr > 0 && !mbar_wait(empty(s), (rr - 1) & 1, abort, p.dev_status)) {
+            ok = false;
+          } else {
+            uint32_t S[4];
+            decode_scales(cs & 0xFFFFu, S[0], S[1]);
+            decode_scales(cs >> 16, S[2], S[3]);
+            const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+            unsigned char* brow = smem + s * kStageBytes + kABytes + r * 128;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {  // 16-byte chunk j holds k = 8j .. 8j+7
+              const uint4 v = dequant_word(words[j], S[j >> 1]);
+              *reinterpret_cast<uint4*>(brow + ((j ^ swz) << 4)) = v;
+            }
+            fence_proxy_async();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(full_b(s));
+          }
+        }
+      }
     }
   } else {
-    // ------------------------------------------------ dequant, then epilogue
-    const int r = threadIdx.x - 64;  // B-tile row 0..255
-    const int64_t nrow = n0 + r;
-    const bool valid = nrow < p.n;
-    const uint8_t* wrow = p.packed + (valid ? nrow : 0) * (p.k / 2);
-    const uint32_t* srow = reinterpret_cast<const uint32_t*>(p.scales + (valid ? nrow : 0) * (p.k / 16));
-    uint4 q0 = make_uint4(0, 0, 0, 0), q1 = make_uint4(0, 0, 0, 0);
-    uint32_t sc = 0;
-    if (valid && nk > 0) {
-      q0 = ld_nc_u4(wrow);
-      q1 = ld_nc_u4(wrow + 16);
-      sc = __ldg(srow);
-    }
-    const uint32_t swz = (uint32_t)(r & 7);
-    bool ok = true;
-    for (int kb = 0; kb < nk; ++kb) {
-      const int s = kb % kStages, rr = kb / kStages;
-      const uint4 c0 = q0, c1 = q1;
-      const uint32_t cs = sc;
-      if (valid && kb + 1 < nk) {  // prefetch the next step's row slice
-        q0 = ld_nc_u4(wrow + (int64_t)(kb + 1) * 32);
-        q1 = ld_nc_u4(wrow + (int64_t)(kb + 1) * 32 + 16);
-        sc = __ldg(srow + kb + 1);
-      }
-      if (rr > 0 && !mbar_wait(empty(s), (rr - 1) & 1, abort, p.dev_status)) {
-        ok = false;
-        break;
-      }
-      uint32_t S[4];
-      decode_scales(cs & 0xFFFFu, S[0], S[1]);
-      decode_scales(cs >> 16, S[2], S[3]);
-      const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-      unsigned char* brow = smem + s * kStageBytes + kABytes + r * 128;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {  // 16-byte chunk j holds k = 8j .. 8j+7
-        const uint4 v = dequant_word(words[j], S[j >> 1]);
-        *reinterpret_cast<uint4*>(brow + ((j ^ swz) << 4)) = v;
-      }
-      fence_proxy_async();
+    // -------------------------------------------------------------- epilogue
+    // warp quadrant q owns TMEM lanes 32q..32q+31 = rows 32q.. of the tile
+    const int q = warp & 3;
+    const float gs = __ldg(p.gscale) * 256.0f;  // g * 2^8 (the dequant fold)
+    for (int it = 0; it < my_tiles; ++it) {
+      const int ab = it & 1;
       __syncwarp();
-      if (lane == 0) mbar_arrive(full_b(s));
-    }
-    // epilogue: warp quadrant q owns TMEM lanes 32q..32q+31 (rows of the tile)
-    __syncwarp();
-    if (ok && mbar_wait(accum_bar, 0, abort, p.dev_status)) {
+      if (!mbar_wait(tmem_full(ab), (it >> 1) & 1, abort, p.dev_status)) break;
       __syncwarp();
       tc_fence_after();
-      const int q = warp & 3, h = (warp - 2) >> 2;
+      int64_t m0, n0;
+      tile_coords(p, (int)blockIdx.x + it * (int)gridDim.x, m0, n0);
       const int64_t row = m0 + 32 * q + lane;
-      const float gs = __ldg(p.gscale) * 256.0f;
 #pragma unroll 1
-      for (int j = 0; j < 4; ++j) {
-        const int col = 128 * h + 32 * j;
+      for (int j = 0; j < BN / 32; ++j) {
+        const int col = 32 * j;
         uint32_t v[32];
-        tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)col, v);
+        tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(ab * BN + col), v);
         if (row < p.m && n0 + col < p.n) {
           uint32_t packed16[16];
 #pragma unroll
@@ -346,6 +396,9 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
                                 packed16[4 * i + 3]);
         }
       }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tmem_empty(ab));
     }
   }
   tc_fence_before();
@@ -397,10 +450,15 @@ int launch_gemm(const void* a, int64_t m, int64_t lda, const nvfp4_weight* w, vo
   p.n = w->n;
   p.k = w->k;
   p.ldc = ldc;
+  p.mtiles = (int)nvfp4::cdiv(m, BM);
+  p.ntiles = (int)nvfp4::cdiv(w->n, BN);
   p.dev_status = dev_status;
   if (nvfp4::occupancy(reinterpret_cast<const void*>(gemm_tcgen05_kernel), kThreads, kSmemBytes) < 1)
     return NVFP4_ERR_CUDA;
-  dim3 grid((unsigned)nvfp4::cdiv(w->n, BN), (unsigned)nvfp4::cdiv(m, BM));
+  const int64_t tiles = (int64_t)p.mtiles * p.ntiles;
+  if (tiles > 0x7FFFFFFF) return NVFP4_ERR_SHAPE;
+  const int sms = nvfp4::sm_count();
+  const unsigned grid = (unsigned)(tiles < sms ? tiles : sms);  // persistent: one CTA per SM
   gemm_tcgen05_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tmap, p);
   if (cudaGetLastError() != cudaSuccess) return NVFP4_ERR_CUDA;
   return NVFP4_OK;
