@@ -43,11 +43,11 @@ constexpr int kStages = 4;
 constexpr int kABytes = BM * BK * 2;  // 16 KB
 constexpr int kBBytes = BN * BK * 2;  // 32 KB
 constexpr int kStageBytes = kABytes + kBBytes;
-constexpr int kDequantWarps = 8;
+constexpr int kDequantWarps = 16;  // two threads per weight row, 32 K-elements each
 constexpr int kEpilogueWarps = 4;
 constexpr int kThreads = (2 + kDequantWarps + kEpilogueWarps) * 32;
 constexpr int kTmemCols = 2 * BN;  // two accumulators: epilogue of one tile overlaps the next
-constexpr int kPrefetch = 3;       // k steps of weight rows in flight per dequant thread
+constexpr int kPrefetch = 4;       // k steps of weight rows in flight per dequant thread
 constexpr size_t kSmemBytes = 1024 /*alignment slack*/ + (size_t)kStages * kStageBytes + 256;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
@@ -306,28 +306,37 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
     }
   } else if (warp < 2 + kDequantWarps) {
     // --------------------------------------------------------------- dequant
-    const int r = threadIdx.x - 64;  // B-tile row 0..255
+    const int d = threadIdx.x - 64;
+    const int r = d >> 1, h = d & 1;  // B-tile row 0..255, K half (32 elements) 0..1
     const uint32_t swz = (uint32_t)(r & 7);
-    uint4 qa[kPrefetch], qb[kPrefetch];
+    uint4 qa[kPrefetch];
     uint32_t qs[kPrefetch];
-    // load cursor over (tile, k step)
-    int lg = 0;
-    auto issue = [&](int i) {
-      const int it = lg / nk, kb = lg - it * nk;
+    // load cursor over (tile, k step): row pointers change once per tile
+    int lt = 0, lkb = 0;
+    const uint8_t* wp = nullptr;
+    const uint16_t* sp = nullptr;
+    bool lvalid = false;
+    auto set_tile = [&](int it) {
       int64_t m0, n0;
       tile_coords(p, (int)blockIdx.x + it * (int)gridDim.x, m0, n0);
       const int64_t nrow = n0 + r;
-      if (nrow < p.n) {
-        const uint8_t* w = p.packed + nrow * (p.k / 2) + (int64_t)kb * 32;
-        qa[i] = ld_nc_u4(w);
-        qb[i] = ld_nc_u4(w + 16);
-        qs[i] = __ldg(reinterpret_cast<const uint32_t*>(p.scales + nrow * (p.k / 16)) + kb);
-      } else {  // rows past n: zero weights (their outputs are not stored)
+      lvalid = nrow < p.n;
+      wp = p.packed + (lvalid ? nrow : 0) * (p.k / 2) + 16 * h;
+      sp = reinterpret_cast<const uint16_t*>(p.scales + (lvalid ? nrow : 0) * (p.k / 16)) + h;
+    };
+    set_tile(0);
+    auto issue = [&](int i) {
+      if (lvalid) {  // rows past n: zero weights (their outputs are not stored)
+        qa[i] = ld_nc_u4(wp + (int64_t)lkb * 32);
+        qs[i] = __ldg(sp + 2 * lkb);
+      } else {
         qa[i] = make_uint4(0, 0, 0, 0);
-        qb[i] = make_uint4(0, 0, 0, 0);
         qs[i] = 0u;
       }
-      ++lg;
+      if (++lkb == nk) {
+        lkb = 0;
+        if (++lt < my_tiles) set_tile(lt);
+      }
     };
 #pragma unroll
     for (int i = 0; i < kPrefetch; ++i)
@@ -339,21 +348,20 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
         const int g = g0 + i;
         if (g < total && ok) {
           const int s = g % kStages, rr = g / kStages;
-          const uint4 c0 = qa[i], c1 = qb[i];
+          const uint4 c0 = qa[i];
           const uint32_t cs = qs[i];
           if (g + kPrefetch < total) issue(i);
           if (rr > 0 && !mbar_wait(empty(s), (rr - 1) & 1, abort, p.dev_status)) {
             ok = false;
           } else {
-            uint32_t S[4];
-            decode_scales(cs & 0xFFFFu, S[0], S[1]);
-            decode_scales(cs >> 16, S[2], S[3]);
-            const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+            uint32_t S0, S1;
+            decode_scales(cs, S0, S1);
+            const uint32_t words[4] = {c0.x, c0.y, c0.z, c0.w};
             unsigned char* brow = smem + s * kStageBytes + kABytes + r * 128;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {  // 16-byte chunk j holds k = 8j .. 8j+7
-              const uint4 v = dequant_word(words[j], S[j >> 1]);
-              *reinterpret_cast<uint4*>(brow + ((j ^ swz) << 4)) = v;
+            for (int j = 0; j < 4; ++j) {  // chunk 4h+j holds k = 32h + 8j .. +7
+              const uint4 v = dequant_word(words[j], j < 2 ? S0 : S1);
+              *reinterpret_cast<uint4*>(brow + (((uint32_t)(4 * h + j) ^ swz) << 4)) = v;
             }
             fence_proxy_async();
             __syncwarp();
