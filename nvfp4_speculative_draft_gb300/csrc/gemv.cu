@@ -171,33 +171,50 @@ template <int M>
 __device__ void build_fragments(const GemvParams& p, uint2* bfrag, float* rms) {
   constexpr int BSTRIDE = 4 * M;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  // 1. inverse RMS per (row, segment)
-  for (int job = warp; job < M * p.nseg; job += kWarps) {
-    const int r = job / p.nseg, s = job % p.nseg;
-    if (p.gamma[s] == nullptr) {
-      if (lane == 0) rms[job] = 1.0f;
-      continue;
-    }
-    const __nv_bfloat16* xr = p.x[s] + (int64_t)r * p.ld[s];
-    float ss = 0.0f;
-    for (int64_t i = (int64_t)lane * 8; i < p.kseg[s]; i += 32 * 8) {
-      if (!NVFP4_GUARD(r < M && s < p.nseg && i + 8 <= p.kseg[s], 1, p.dev_status)) continue;
-      const uint4 v = *reinterpret_cast<const uint4*>(xr + i);
-      const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+  // 1. inverse RMS per (row, segment) job.  The CTA's warps split each job's
+  //    k range (all 16 warps for a single job), four 16-byte loads in flight
+  //    per lane; per-(job, warp) partial sums are combined in a fixed order,
+  //    so the result does not depend on timing.
+  float* part = rms + 16;  // [16 jobs][kWarps]
+  const int J = M * p.nseg;
+  const int wpj = J >= kWarps ? 1 : kWarps / J;  // warps per job
+  const int jpp = kWarps / wpj;                  // jobs per pass
+  for (int j0 = 0; j0 < J; j0 += jpp) {
+    const int job = j0 + warp / wpj, wj = warp % wpj;
+    if (job < J) {
+      const int r = job / p.nseg, s = job % p.nseg;
+      float ss = 0.0f;
+      if (p.gamma[s] != nullptr) {
+        const __nv_bfloat16* xr = p.x[s] + (int64_t)r * p.ld[s];
+#pragma unroll 4
+        for (int64_t i = (int64_t)(wj * 32 + lane) * 8; i < p.kseg[s]; i += (int64_t)wpj * 256) {
+          if (!NVFP4_GUARD(r < M && s < p.nseg && i + 8 <= p.kseg[s], 1, p.dev_status)) continue;
+          const uint4 v = *reinterpret_cast<const uint4*>(xr + i);
+          const uint32_t u[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float a = __uint_as_float(u[j] << 16), b = __uint_as_float(u[j] & 0xFFFF0000u);
-        ss = fmaf(a, a, ss);
-        ss = fmaf(b, b, ss);
+          for (int j = 0; j < 4; ++j) {
+            const float a = __uint_as_float(u[j] << 16), b = __uint_as_float(u[j] & 0xFFFF0000u);
+            ss = fmaf(a, a, ss);
+            ss = fmaf(b, b, ss);
+          }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
       }
+      if (lane == 0) part[job * kWarps + wj] = ss;
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
-    if (lane == 0) rms[job] = 1.0f / sqrtf(ss / (float)p.kseg[s] + p.eps[s]);
+  }
+  __syncthreads();
+  if (tid < J) {
+    const int s = tid % p.nseg;
+    float ss = 0.0f;
+    for (int w = 0; w < wpj; ++w) ss += part[tid * kWarps + w];
+    rms[tid] = p.gamma[s] == nullptr ? 1.0f : 1.0f / sqrtf(ss / (float)p.kseg[s] + p.eps[s]);
   }
   __syncthreads();
   // 2. fragments
   const int64_t gpr = (int64_t)p.nchunks * (kChunk / 8);  // 8-element groups per row
+#pragma unroll 4
   for (int64_t gi = tid; gi < (int64_t)M * gpr; gi += kThreads) {
     const int r = (int)(gi / gpr);
     const int64_t kk = (gi % gpr) * 8;
@@ -233,9 +250,18 @@ __device__ void build_fragments(const GemvParams& p, uint2* bfrag, float* rms) {
   }
 }
 
-// Named barrier over the `count` threads of one tile group (ids 1..15).
-__device__ __forceinline__ void group_sync(int id, int count) {
+// Named barriers over the `count` threads of one tile group: the split-K
+// partials go from the ks-1 producer warps to the tile's first warp through a
+// "full" barrier (ids 1..4: producers arrive, the consumer waits); an "empty"
+// barrier (ids 5..8: the consumer arrives after reading tile t, producers wait
+// on it before publishing tile t+1) keeps every producer from arriving twice
+// on a full barrier before it completes.  Split factors are 1, 4, 8 or 16, so
+// at most 4 tile groups share a CTA.
+__device__ __forceinline__ void bar_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+__device__ __forceinline__ void bar_arrive(int id, int count) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 // ------------------------------------------------------------------ kernel
@@ -254,8 +280,9 @@ gemv_kernel(const __grid_constant__ GemvParams p) {
   uint2* bfrag = reinterpret_cast<uint2*>(smem);
   const size_t bbytes = (size_t)p.nchunks * 8 * BSTRIDE * sizeof(uint2);
   float* red = reinterpret_cast<float*>(smem + bbytes);                // [2][kWarps][32][4]
-  float* rms = red + 2 * kWarps * 32 * 4;                              // [16]
-  unsigned long long* kred = reinterpret_cast<unsigned long long*>(rms + 16);  // [kWarps][32][2]
+  float* rms = red + 2 * kWarps * 32 * 4;                    // [16] + partial sums [16][kWarps]
+  unsigned long long* kred =
+      reinterpret_cast<unsigned long long*>(rms + 16 + 16 * kWarps);  // [kWarps][32][2]
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, t = lane & 3;
@@ -334,16 +361,21 @@ gemv_kernel(const __grid_constant__ GemvParams p) {
     }
     if (ks > 1) {
       float* rb = red + (size_t)(it & 1) * kWarps * 32 * 4;
+      const int full_id = 1 + slot, empty_id = 5 + slot;  // slot < 4 when ks >= 4
       if (kpart != 0) {
+        // The consumer has finished tile it-1 (so no producer can arrive on the
+        // full barrier twice before it completes).
+        if (it >= 1) bar_sync(empty_id, ks * 32);
         float* mine = rb + (warp * 32 + lane) * 4;
         mine[0] = acc[0]; mine[1] = acc[1]; mine[2] = acc[2]; mine[3] = acc[3];
-      }
-      group_sync(1 + slot, ks * 32);
-      if (kpart == 0) {
+        bar_arrive(full_id, ks * 32);
+      } else {
+        bar_sync(full_id, ks * 32);
         for (int j = 1; j < ks; ++j) {
           const float* o = rb + ((warp + j) * 32 + lane) * 4;
           acc[0] += o[0]; acc[1] += o[1]; acc[2] += o[2]; acc[3] += o[3];
         }
+        bar_arrive(empty_id, ks * 32);
       }
     }
     if (kpart == 0 && tile < p.ntiles) {
@@ -392,6 +424,9 @@ gemv_kernel(const __grid_constant__ GemvParams p) {
       }
     }
   }
+
+  if (ks > 1 && kpart != 0 && n_iter > 0)  // match the consumer's last "empty" arrival
+    bar_sync(5 + slot, ks * 32);
 
   if (p.keys == nullptr) return;
   // argmax: lanes sharing t hold the same two rows of the batch
@@ -472,7 +507,8 @@ int launch_gemv(const w4a16_act_segment* seg, int nseg, int m, const nvfp4_weigh
   p.nfull = (int)(w->k / kChunk);
 
   const size_t bbytes = (size_t)p.nchunks * 8 * 4 * m * sizeof(uint2);
-  const size_t smem = bbytes + 2 * kWarps * 32 * 4 * sizeof(float) + 16 * sizeof(float) +
+  const size_t smem = bbytes + 2 * kWarps * 32 * 4 * sizeof(float) +
+                      (16 + 16 * kWarps) * sizeof(float) +
                       kWarps * 32 * 2 * sizeof(unsigned long long);
   KernelFn fn = kernel_for(m);
   const int occ = nvfp4::occupancy(reinterpret_cast<const void*>(fn), kThreads, smem);
@@ -483,7 +519,7 @@ int launch_gemv(const w4a16_act_segment* seg, int nseg, int m, const nvfp4_weigh
   // groups to stream, keeping at least 4 full chunks per warp.
   int ks = 1;
   while (ks < kWarps && nvfp4::cdiv(p.ntiles, kWarps / ks) < 4 * slots && p.nfull / (2 * ks) >= 4)
-    ks *= 2;
+    ks = ks == 1 ? 4 : 2 * ks;
   p.ks = ks;
   const int64_t ngroups = nvfp4::cdiv(p.ntiles, kWarps / ks);
   const int64_t grid = ngroups < slots ? ngroups : slots;
