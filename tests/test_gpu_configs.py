@@ -1,0 +1,180 @@
+"""GPU parity at the full workload sizes, in the launch configuration the
+benchmark times, against the CPU oracle (run on all host cores from here; the
+oracle's own code is unchanged).  Where the oracle cannot cover every output
+in seconds, outputs are sampled (seeded) and checked one by one.
+
+Bars as in test_gpu_parity: codes/scales/absmax/g bit-exact; FP32 logits
+within 1e-3 * S + 1e-6; BF16 outputs the same plus one BF16 ulp; argmax equal
+to the first maximum of the GPU's own logits and to the oracle's index when
+the oracle's top-2 gap exceeds the tolerances.
+"""
+import os
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+TOL_REL, TOL_ABS = 1e-3, 1e-6
+THREADS = max(1, min(32, os.cpu_count() or 1))
+
+
+def nd():
+    import nvfp4_speculative_draft_gb300 as m
+    return m
+
+
+def par_quantize_rows(wb, rows, g):
+    chunks = np.array_split(np.asarray(rows), THREADS)
+    with ThreadPoolExecutor(THREADS) as ex:
+        parts = list(ex.map(lambda r: oracle.quantize_rows(wb, r, g), [c for c in chunks if len(c)]))
+    return np.concatenate([p for p, _ in parts]), np.concatenate([s for _, s in parts])
+
+
+def par_gemv(a, packed, scales, g):
+    n = packed.shape[0]
+    bounds = np.linspace(0, n, THREADS + 1).astype(int)
+    jobs = [(bounds[i], bounds[i + 1] - bounds[i]) for i in range(THREADS) if bounds[i + 1] > bounds[i]]
+    with ThreadPoolExecutor(THREADS) as ex:
+        res = list(ex.map(lambda j: oracle.gemv(a, packed, scales, g, n0=j[0], nn=j[1]), jobs))
+    return np.concatenate([y for y, _ in res], axis=1), np.concatenate([s for _, s in res], axis=1)
+
+
+def check_gpu_quant(wq, amax, wb, sample_rows=None):
+    """GPU quantisation vs the oracle: absmax and g exactly, then every row
+    (or the sampled rows) bit-exact."""
+    a_ref = oracle.global_absmax(wb)
+    g_ref = oracle.global_scale(a_ref)
+    assert amax.item() == a_ref
+    assert wq.global_scale.item() == float(g_ref)
+    rows = np.arange(wb.shape[0]) if sample_rows is None else np.asarray(sample_rows)
+    p_ref, s_ref = par_quantize_rows(wb, rows, g_ref)
+    gp = wq.packed[torch.from_numpy(rows).to(wq.packed.device)].cpu().numpy()
+    gs = wq.scales[torch.from_numpy(rows).to(wq.scales.device)].cpu().numpy()
+    assert np.array_equal(gs, s_ref), "scale bytes differ"
+    assert np.array_equal(gp, p_ref), "packed codes differ"
+    return g_ref
+
+
+def check_logits_and_argmax(lg, idx, y, sabs):
+    err = np.abs(lg.astype(np.float64) - y)
+    tol = TOL_REL * sabs + TOL_ABS
+    assert np.all(err <= tol), f"{int((err > tol).sum())} logits out of tolerance"
+    for r in range(y.shape[0]):
+        i = int(idx[r])
+        assert i == oracle.argmax(lg[r].astype(np.float64))
+        j = oracle.argmax(y[r])
+        top = np.partition(-y[r], 1)[:2]
+        if (-top[0]) - (-top[1]) > 2 * tol[r].max():
+            assert i == j
+        else:
+            assert y[r, i] >= y[r, j] - tol[r, j] - tol[r, i]
+
+
+def test_tiny_config(dev):
+    m = nd()
+    case = workloads.tiny()
+    wq, amax = m.nvfp4_quantize(case.w.to(dev))
+    wb = workloads.bits(case.w)
+    g = check_gpu_quant(wq, amax, wb)
+    x = case.segments[0][0]
+    logits, idx = m.w4a16_gemv_argmax([(x.to(dev), None)], wq)
+    torch.cuda.synchronize()
+    y, sabs = oracle.gemv(workloads.bits(x), wq.packed.cpu().numpy(), wq.scales.cpu().numpy(), g)
+    check_logits_and_argmax(logits.cpu().numpy(), idx.cpu().numpy(), y, sabs)
+
+
+def test_lm_head_config_full(dev):
+    """32768 x 4096 reduced-vocab head with 1% outlier rows; RMSNorm + GEMV +
+    argmax at M=1 for three of the seeded hidden rows."""
+    m = nd()
+    case = workloads.lm_head_m1(rows=3, device=dev)
+    wq, amax = m.nvfp4_quantize(case.w)
+    wb = workloads.bits(case.w)
+    g = check_gpu_quant(wq, amax, wb)
+    h, gamma = case.segments[0]
+    pk, sc = wq.packed.cpu().numpy(), wq.scales.cpu().numpy()
+    for r in range(3):
+        logits, idx = m.w4a16_gemv_argmax([(h[r:r + 1], gamma, 1e-6)], wq)
+        torch.cuda.synchronize()
+        a = oracle.rmsnorm_concat([(workloads.bits(h[r:r + 1]), workloads.bits(gamma), 1e-6)], 1)
+        y, sabs = par_gemv(a, pk, sc, g)
+        check_logits_and_argmax(logits.cpu().numpy(), idx.cpu().numpy(), y, sabs)
+
+
+def test_propose_config_full_width(dev):
+    """151936 x 5120 head: quantiser on sampled rows, M=1 logits + argmax over
+    every row, M=8 logits on sampled rows and argmax of the GPU's own logits."""
+    m = nd()
+    case = workloads.propose_m8(device=dev)
+    wq, amax = m.nvfp4_quantize(case.w)
+    wb = workloads.bits(case.w)
+    rng = np.random.default_rng(11)
+    rows = np.unique(np.concatenate([rng.integers(0, 151936, 3000), [0, 1, 151935]]))
+    g = check_gpu_quant(wq, amax, wb, sample_rows=rows)
+    del wb
+    x = case.segments[0][0]
+    pk, sc = wq.packed.cpu().numpy(), wq.scales.cpu().numpy()
+    logits, idx = m.w4a16_gemv_argmax([(x[:1], None)], wq)
+    torch.cuda.synchronize()
+    y, sabs = par_gemv(workloads.bits(x[:1]), pk, sc, g)
+    check_logits_and_argmax(logits.cpu().numpy(), idx.cpu().numpy(), y, sabs)
+    for mm in (2, 4, 8):
+        logits, idx = m.w4a16_gemv_argmax([(x[:mm].contiguous(), None)], wq)
+        torch.cuda.synchronize()
+        lg = logits.cpu().numpy()
+        ys, ss = oracle.gemv(workloads.bits(x[:mm]), pk[rows], sc[rows], g)
+        err = np.abs(lg[:, rows].astype(np.float64) - ys)
+        assert np.all(err <= TOL_REL * ss + TOL_ABS)
+        for r in range(mm):
+            assert int(idx[r]) == oracle.argmax(lg[r].astype(np.float64))
+
+
+@pytest.mark.parametrize("mm", [1, 4, 8])
+def test_fc_combiner_config_full(dev, mm):
+    """5120 x 10240 fc over RMSNorm(e) ++ RMSNorm(h), BF16 output, every output."""
+    m = nd()
+    case = workloads.fc_combiner(device=dev)
+    wq, amax = m.nvfp4_quantize(case.w)
+    g = float(wq.global_scale.item())
+    (e, ge), (h, gh) = case.segments
+    out = m.w4a16_gemv([(e[:mm].contiguous(), ge, 1e-6), (h[:mm].contiguous(), gh, 1e-6)], wq,
+                       out_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    a = oracle.rmsnorm_concat([(workloads.bits(e[:mm]), workloads.bits(ge), 1e-6),
+                               (workloads.bits(h[:mm]), workloads.bits(gh), 1e-6)], mm)
+    y, sabs = par_gemv(a, wq.packed.cpu().numpy(), wq.scales.cpu().numpy(), np.float32(g))
+    got = out.float().cpu().numpy().astype(np.float64)
+    assert np.all(np.abs(got - y) <= TOL_REL * sabs + TOL_ABS + np.abs(y) * 2.0 ** -8)
+
+
+def test_prefill_gemm_config_sampled(dev):
+    """2048 x 17408 x 5120 prefill GEMM: quantiser bit-exact on every row, and
+    8192 sampled outputs plus two full rows and two full columns."""
+    m = nd()
+    case = workloads.prefill_gemm(device=dev)
+    wq, amax = m.nvfp4_quantize(case.w)
+    wb = workloads.bits(case.w)
+    g = check_gpu_quant(wq, amax, wb)
+    c = m.w4a16_gemm(case.a, wq)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(12)
+    rows = np.concatenate([rng.integers(0, 2048, 8192), np.full(17408, 5), np.full(17408, 2047),
+                           np.arange(2048), np.arange(2048)])
+    cols = np.concatenate([rng.integers(0, 17408, 8192), np.arange(17408), np.arange(17408),
+                           np.full(2048, 0), np.full(2048, 17407)])
+    ab = workloads.bits(case.a)
+    pk, sc = wq.packed.cpu().numpy(), wq.scales.cpu().numpy()
+    parts = np.array_split(np.arange(rows.size), THREADS)
+    with ThreadPoolExecutor(THREADS) as ex:
+        res = list(ex.map(lambda ix: oracle.gemm_pairs(ab, pk, sc, g, rows[ix], cols[ix]), parts))
+    exact = np.concatenate([e for e, _ in res])
+    sabs = np.concatenate([s for _, s in res])
+    got = c.float().cpu().numpy()[rows, cols].astype(np.float64)
+    bad = np.abs(got - exact) > TOL_REL * sabs + TOL_ABS + np.abs(exact) * 2.0 ** -8
+    assert not bad.any(), f"{int(bad.sum())} sampled outputs out of tolerance"
