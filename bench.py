@@ -388,6 +388,23 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def recorded_traffic(key):
+    """DRAM bytes per launch from the committed ncu capture, or None when the
+    kernel's source has changed since the counters were taken."""
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.txt")) as f:
+            for line in f:
+                parts = line.split()
+                if len(parts) == 4 and parts[0] == key:
+                    src = open(os.path.join(ROOT, parts[2]), "rb").read()
+                    if hashlib.sha256(src).hexdigest()[:16] == parts[3]:
+                        return int(parts[1])
+    except OSError:
+        pass
+    return None
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -420,12 +437,7 @@ def main():
     per_launch_us = r["ms_step"] * 1e3 / r["calls"]
     achieved = r["bytes_per_call"] / (per_launch_us * 1e-6) / 1e9
     e2e_v = r["calls"] * r["bytes_per_call"] / (r["e2e_ms_step"] * 1e-3) / 1e9 * world
-    traffic = None
-    try:
-        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
-            traffic = json.load(f).get("gemv_kernel_lm_head_m1")
-    except Exception:
-        pass
+    traffic = recorded_traffic("gemv_kernel_lm_head_m1")
     line = {
         "metric": METRIC, "value": gbps, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": r["ms_step"], "higher_is_better": True,
