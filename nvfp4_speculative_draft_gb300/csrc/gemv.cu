@@ -77,50 +77,50 @@ __device__ __forceinline__ uint4 ld_stream_u4(const void* p) {
   return v;
 }
 
-__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
+__device__ __forceinline__ uint32_t f16x2_mul(uint32_t a, uint32_t b) {
   uint32_t d;
-  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
   return d;
 }
 
-__device__ __forceinline__ void mma_bf16_16816(float (&c)[4], uint32_t a0, uint32_t a1,
-                                               uint32_t a2, uint32_t a3, uint32_t b0,
-                                               uint32_t b1) {
+__device__ __forceinline__ void mma_f16_16816(float (&c)[4], uint32_t a0, uint32_t a1,
+                                              uint32_t a2, uint32_t a3, uint32_t b0,
+                                              uint32_t b1) {
   asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
       "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Two E4M3 block scales (low byte first) -> BF16 patterns of scale * 2^118,
-// each replicated into both halves of a bf16x2.
+// Two E4M3 block scales (low byte first) -> F16 (exact: E4M3 values are F16
+// normals), each replicated into both halves of an f16x2.
 __device__ __forceinline__ void decode_scales(uint32_t s2, uint32_t& lo, uint32_t& hi) {
   const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)s2, __NV_E4M3);
-  // F16 -> BF16 by a 3-bit right shift: the exponent field lands unbiased-by-112,
-  // i.e. the BF16 pattern holds value * 2^-112 (normal; zero stays zero).  The
-  // F16 images of E4M3 values have their low 7 mantissa bits clear, so the shift
-  // moves nothing across the half boundary.
-  uint32_t v = ((uint32_t)h.x | ((uint32_t)h.y << 16)) >> 3;
-  v = bf16x2_mul(v, 0x79007900u);  // * 2^115
-  v = bf16x2_mul(v, 0x79007900u);  // * 2^115  -> scale * 2^118
+  const uint32_t v = (uint32_t)h.x | ((uint32_t)h.y << 16);
   lo = __byte_perm(v, 0, 0x1010);
   hi = __byte_perm(v, 0, 0x3232);
 }
 
-// E2M1 nibble pair -> bf16x2 pattern (value * 2^-126).  x holds one nibble in
-// each 16-bit half at bit offset 0 (mul = 0x1040) or 4 (mul = 0x104): the
-// multiply makes two non-overlapping shifted copies, one placing the sign at
-// bit 15, one placing the 3 magnitude bits at bits 8..6 (exponent LSBs +
-// mantissa MSB); the mask keeps exactly those.
-__device__ __forceinline__ uint32_t e2m1_pair(uint32_t x, uint32_t mul) {
-  return (x * mul) & 0x81C081C0u;
+// The 8 E2M1 codes of word q -> 4 f16x2 (nibbles 0|1, 2|3, 4|5, 6|7; the even
+// nibble in the low half) by the hardware conversion, exact.
+__device__ __forceinline__ void e2m1_word_to_f16(uint32_t q, uint32_t& h0, uint32_t& h1,
+                                                 uint32_t& h2, uint32_t& h3) {
+  asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n"
+      " cvt.rn.f16x2.e2m1x2 %0, b0;\n cvt.rn.f16x2.e2m1x2 %1, b1;\n"
+      " cvt.rn.f16x2.e2m1x2 %2, b2;\n cvt.rn.f16x2.e2m1x2 %3, b3;\n}"
+      : "=r"(h0), "=r"(h1), "=r"(h2), "=r"(h3)
+      : "r"(q));
 }
 
 // One 128-element chunk of one lane: weights qg (row g) / qh (row g + 8),
 // scale pairs sg / sh, B fragments from shared memory at bfrag[j * BSTRIDE]
 // for MMA j (lanes whose batch column is >= M read a duplicate of a valid
 // column: MMA columns are independent and those outputs are discarded).
+// Lane (g, t) holds K elements 32t .. 32t+31 of the chunk; word w of its
+// 16-byte load covers 32t + 8w .. +7, and MMA 2w+u takes the pairs of
+// elements 4u .. 4u+3 of that word, so the MMA's column c = 2t + e + 8h is
+// element 32t + 8w + 4u + 2h + e: a B fragment is 4 consecutive activations.
 template <int BSTRIDE>
 __device__ __forceinline__ void chunk_mma(float (&acc)[4], const uint4& qg, const uint4& qh,
                                           uint32_t sg, uint32_t sh, const uint2* bfrag) {
@@ -132,20 +132,15 @@ __device__ __forceinline__ void chunk_mma(float (&acc)[4], const uint4& qg, cons
 #pragma unroll
   for (int w = 0; w < 4; ++w) {
     const uint32_t sG = Sg[w >> 1], sH = Sh[w >> 1];
-    const uint32_t g0 = wg[w], g8 = wg[w] >> 8;
-    const uint32_t h0 = wh[w], h8 = wh[w] >> 8;
-    const uint32_t ag0 = bf16x2_mul(e2m1_pair(g0 & 0x000F000Fu, 0x1040u), sG);  // nibbles 0,4
-    const uint32_t ag1 = bf16x2_mul(e2m1_pair(g0 & 0x00F000F0u, 0x0104u), sG);  // 1,5
-    const uint32_t ag2 = bf16x2_mul(e2m1_pair(g8 & 0x000F000Fu, 0x1040u), sG);  // 2,6
-    const uint32_t ag3 = bf16x2_mul(e2m1_pair(g8 & 0x00F000F0u, 0x0104u), sG);  // 3,7
-    const uint32_t ah0 = bf16x2_mul(e2m1_pair(h0 & 0x000F000Fu, 0x1040u), sH);
-    const uint32_t ah1 = bf16x2_mul(e2m1_pair(h0 & 0x00F000F0u, 0x0104u), sH);
-    const uint32_t ah2 = bf16x2_mul(e2m1_pair(h8 & 0x000F000Fu, 0x1040u), sH);
-    const uint32_t ah3 = bf16x2_mul(e2m1_pair(h8 & 0x00F000F0u, 0x0104u), sH);
+    uint32_t g0, g1, g2, g3, h0, h1, h2, h3;
+    e2m1_word_to_f16(wg[w], g0, g1, g2, g3);
+    e2m1_word_to_f16(wh[w], h0, h1, h2, h3);
     const uint2 b0 = bfrag[(2 * w) * BSTRIDE];
-    mma_bf16_16816(acc, ag0, ah0, ag1, ah1, b0.x, b0.y);
+    mma_f16_16816(acc, f16x2_mul(g0, sG), f16x2_mul(h0, sH), f16x2_mul(g1, sG),
+                  f16x2_mul(h1, sH), b0.x, b0.y);
     const uint2 b1 = bfrag[(2 * w + 1) * BSTRIDE];
-    mma_bf16_16816(acc, ag2, ah2, ag3, ah3, b1.x, b1.y);
+    mma_f16_16816(acc, f16x2_mul(g2, sG), f16x2_mul(h2, sH), f16x2_mul(g3, sG),
+                  f16x2_mul(h3, sH), b1.x, b1.y);
   }
 }
 
@@ -212,7 +207,15 @@ __device__ void build_fragments(const GemvParams& p, uint2* bfrag, float* rms) {
     rms[tid] = p.gamma[s] == nullptr ? 1.0f : 1.0f / sqrtf(ss / (float)p.kseg[s] + p.eps[s]);
   }
   __syncthreads();
-  // 2. fragments
+  // 2. normalised BF16 activations into the fragment slots.  The 8 activations
+  //    at kk = 128c + 32t + 8w of row m fill MMA 8c+2w (elements 0..3) and MMA
+  //    8c+2w+1 (elements 4..7) of lane 4m + t.  Positions past k are zero.
+  //    The largest magnitude of each row is collected on the way (the BF16
+  //    magnitude bits order like the values).
+  unsigned int* rowmax = reinterpret_cast<unsigned int*>(part + 16 * kWarps);  // [8]
+  float* rowscale = reinterpret_cast<float*>(rowmax + 8);                        // [8]
+  if (tid < 8) rowmax[tid] = 0u;
+  __syncthreads();
   const int64_t gpr = (int64_t)p.nchunks * (kChunk / 8);  // 8-element groups per row
 #pragma unroll 4
   for (int64_t gi = tid; gi < (int64_t)M * gpr; gi += kThreads) {
@@ -236,17 +239,45 @@ __device__ void build_fragments(const GemvParams& p, uint2* bfrag, float* rms) {
           a[j] = pack_bf16x2(lo, hi);
         }
       }
+      const uint32_t mx = __vmaxu2(__vmaxu2(a[0] & 0x7FFF7FFFu, a[1] & 0x7FFF7FFFu),
+                                   __vmaxu2(a[2] & 0x7FFF7FFFu, a[3] & 0x7FFF7FFFu));
+      const uint32_t m1 = max(mx & 0xFFFFu, mx >> 16);
+      if (m1 != 0u) atomicMax(rowmax + r, m1);
     }
     const int c = (int)(kk / kChunk), t = (int)((kk % kChunk) / 32), w = (int)((kk % 32) / 8);
     const int L = 4 * r + t;
     if (!NVFP4_GUARD((int64_t)(8 * c + 2 * w + 1) * BSTRIDE + L < (int64_t)p.nchunks * 8 * BSTRIDE &&
                          L < BSTRIDE, 3, p.dev_status))
       continue;
-    // element e of the group lives in half (e & 1) of a[e >> 1]
-    const uint32_t e0 = a[0] & 0xFFFFu, e1 = a[0] >> 16, e2 = a[1] & 0xFFFFu, e3 = a[1] >> 16;
-    const uint32_t e4 = a[2] & 0xFFFFu, e5 = a[2] >> 16, e6 = a[3] & 0xFFFFu, e7 = a[3] >> 16;
-    bfrag[(int64_t)(8 * c + 2 * w) * BSTRIDE + L] = make_uint2(e0 | (e4 << 16), e1 | (e5 << 16));
-    bfrag[(int64_t)(8 * c + 2 * w + 1) * BSTRIDE + L] = make_uint2(e2 | (e6 << 16), e3 | (e7 << 16));
+    bfrag[(int64_t)(8 * c + 2 * w) * BSTRIDE + L] = make_uint2(a[0], a[1]);
+    bfrag[(int64_t)(8 * c + 2 * w + 1) * BSTRIDE + L] = make_uint2(a[2], a[3]);
+  }
+  __syncthreads();
+  // 3. per-row power-of-two scale 2^e so that max |a| * 2^e lies in [2^14, 2^15):
+  //    every BF16 activation within 2^-31 of the row's largest magnitude then
+  //    converts to FP16 exactly (8 significant bits, FP16 normal range).
+  if (tid < M) {
+    const int ef = (int)(rowmax[tid] >> 7);  // biased BF16 exponent of the row maximum
+    int e = rowmax[tid] == 0u ? 0 : 14 - (ef == 0 ? -126 : ef - 127);
+    e = e < -120 ? -120 : (e > 120 ? 120 : e);
+    rowscale[tid] = ldexpf(1.0f, e);
+    rowscale[8 + tid] = ldexpf(1.0f, -e);  // undone on the FP32 sum
+  }
+  __syncthreads();
+  // 4. BF16 -> scaled FP16 in place
+  const int64_t slots = (int64_t)p.nchunks * 8 * BSTRIDE;
+  for (int64_t i = tid; i < slots; i += kThreads) {
+    const float sc = rowscale[(int)(i % BSTRIDE) / 4];
+    uint2 v = bfrag[i];
+    const uint32_t u[2] = {v.x, v.y};
+    uint32_t o[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const __half2 h = __floats2half2_rn(__uint_as_float(u[j] << 16) * sc,
+                                          __uint_as_float(u[j] & 0xFFFF0000u) * sc);
+      o[j] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    bfrag[i] = make_uint2(o[0], o[1]);
   }
 }
 
@@ -281,8 +312,9 @@ gemv_kernel(const __grid_constant__ GemvParams p) {
   const size_t bbytes = (size_t)p.nchunks * 8 * BSTRIDE * sizeof(uint2);
   float* red = reinterpret_cast<float*>(smem + bbytes);                // [2][kWarps][32][4]
   float* rms = red + 2 * kWarps * 32 * 4;                    // [16] + partial sums [16][kWarps]
+  // after rms: partial sums [16][kWarps], row maxima [8], row scales [16]
   unsigned long long* kred =
-      reinterpret_cast<unsigned long long*>(rms + 16 + 16 * kWarps);  // [kWarps][32][2]
+      reinterpret_cast<unsigned long long*>(rms + 16 + 16 * kWarps + 8 + 16);  // [kWarps][32][2]
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, t = lane & 3;
@@ -332,7 +364,11 @@ gemv_kernel(const __grid_constant__ GemvParams p) {
   if (n_iter > 0 || blockIdx.x == 0) build_fragments<M>(p, bfrag, rms);
   __syncthreads();
 
-  const float gs = __ldg(p.gscale) * 256.0f;  // g * 2^8 (the dequant fold)
+  const float gsc = __ldg(p.gscale);
+  // inverse activation scales of this lane's two batch columns (2t, 2t+1)
+  const float* rowscale = reinterpret_cast<const float*>(
+      reinterpret_cast<const unsigned int*>(rms + 16 + 16 * kWarps) + 8);
+  const float inv0 = rowscale[8 + min(2 * t, M - 1)], inv1 = rowscale[8 + min(2 * t + 1, M - 1)];
   const uint2* bbase = bfrag + (lane % BSTRIDE);
   // running argmax keys of this lane's two batch columns live in shared memory
   unsigned long long* best = kred + (warp * 32 + lane) * 2;
@@ -387,7 +423,7 @@ gemv_kernel(const __grid_constant__ GemvParams p) {
         for (int e = 0; e < 2; ++e) {
           const int mm = 2 * t + e;
           if (mm >= M) continue;
-          const float v = acc[2 * h + e] * gs;
+          const float v = (acc[2 * h + e] * (e ? inv1 : inv0)) * gsc;
           if (p.y != nullptr &&
               NVFP4_GUARD(mm < M && rows[h] < p.n && rows[h] < p.ldy, 6, p.dev_status)) {
             if (p.y_dtype == NVFP4_DTYPE_F32)
@@ -508,7 +544,7 @@ int launch_gemv(const w4a16_act_segment* seg, int nseg, int m, const nvfp4_weigh
 
   const size_t bbytes = (size_t)p.nchunks * 8 * 4 * m * sizeof(uint2);
   const size_t smem = bbytes + 2 * kWarps * 32 * 4 * sizeof(float) +
-                      (16 + 16 * kWarps) * sizeof(float) +
+                      (16 + 16 * kWarps + 8 + 16) * sizeof(float) +
                       kWarps * 32 * 2 * sizeof(unsigned long long);
   KernelFn fn = kernel_for(m);
   const int occ = nvfp4::occupancy(reinterpret_cast<const void*>(fn), kThreads, smem);
