@@ -1,6 +1,8 @@
 // api.cu -- the C ABI: argument validation on the host, then the launchers.
 // Nothing here allocates, synchronises or keeps state beyond a cached SM count.
 
+#include <cudaTypedefs.h>
+
 #include <mutex>
 
 #include "common.cuh"
@@ -87,6 +89,28 @@ int check_segments(const w4a16_act_segment* seg, int nseg, int m, int64_t k) {
   }
   if (total != k) return NVFP4_ERR_SHAPE;
   return NVFP4_OK;
+}
+
+bool encode_tiled(CUtensorMap* map, CUtensorMapDataType type, cuuint32_t rank, void* addr,
+                  const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box,
+                  const cuuint32_t* elem_strides, CUtensorMapSwizzle swizzle) {
+  static std::mutex mu;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (fn == nullptr) {
+      void* ptr = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                           &q) == cudaSuccess &&
+          q == cudaDriverEntryPointSuccess)
+        fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+  }
+  if (fn == nullptr) return false;
+  return fn(map, type, rank, addr, dims, strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace nvfp4

@@ -2,6 +2,7 @@
 // the public header; nothing here is shared with the CPU oracle).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
@@ -42,6 +43,13 @@ int sm_count();
 // runtime; later queries are served from a table, so calls made while a stream
 // is being captured into a CUDA graph issue no CUDA API calls here.
 int occupancy(const void* func, int threads, size_t smem);
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no -lcuda);
+// false if the entry point is unavailable or the encoder rejects the map.
+// Interleave none, 256-byte L2 promotion, out-of-bounds elements read as zero.
+bool encode_tiled(CUtensorMap* map, CUtensorMapDataType type, cuuint32_t rank, void* addr,
+                  const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box,
+                  const cuuint32_t* elem_strides, CUtensorMapSwizzle swizzle);
 
 // Host-side argument checks shared by the entry points (status codes of
 // nvfp4draft.h).

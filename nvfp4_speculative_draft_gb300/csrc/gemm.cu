@@ -30,9 +30,6 @@
 // its TMEM.
 #include <cuda.h>
 #include <cuda_fp8.h>
-#include <cudaTypedefs.h>
-
-#include <mutex>
 
 #include "common.cuh"
 
@@ -419,35 +416,17 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
   }
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static std::mutex mu;
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  std::lock_guard<std::mutex> lock(mu);
-  if (fn == nullptr) {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  }
-  return fn;
-}
-
 }  // namespace
 
 int launch_gemm(const void* a, int64_t m, int64_t lda, const nvfp4_weight* w, void* c,
                 int64_t ldc, int32_t* dev_status, cudaStream_t stream) {
-  PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
-  if (enc == nullptr) return NVFP4_ERR_CUDA;
   CUtensorMap tmap;
   const cuuint64_t dims[2] = {(cuuint64_t)w->k, (cuuint64_t)m};
   const cuuint64_t strides[1] = {(cuuint64_t)lda * 2};
   const cuuint32_t box[2] = {BK, BM};
   const cuuint32_t estr[2] = {1, 1};
-  if (enc(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(a), dims, strides, box, estr,
-          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+  if (!nvfp4::encode_tiled(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(a), dims,
+                           strides, box, estr, CU_TENSOR_MAP_SWIZZLE_128B))
     return NVFP4_ERR_CUDA;
   GemmParams p;
   p.packed = w->packed;

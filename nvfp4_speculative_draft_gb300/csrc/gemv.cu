@@ -9,40 +9,45 @@
 //     argmax[m] = lowest n with y[m, n] maximal (NaN never wins)
 //
 // Design.  The kernel is bound by streaming the packed weights (0.5625 byte per
-// weight incl. scales) from HBM.  On CUDA cores an 8-row batch would need 8 FP32
-// FMAs per weight on top of the dequantisation, more instruction issue than the
-// SMs have at HBM speed; so the inner product runs on the tensor cores with the
-// legacy warp-level mma.sync m16n8k16 (BF16 in, FP32 accumulate) fed straight
-// from registers: the 16-row A side is a weight tile dequantised in registers,
-// the 8-column B side holds the (up to 8) activation rows.  That costs the same
-// instructions per weight for m = 1..8.
-//
-//   * weights: each lane streams 16-byte vectors (ld.global.nc, L1 no-allocate)
-//     of two rows, PF chunks of 128 K-elements ahead in registers;
-//   * dequantisation: E2M1 nibbles -> BF16 bit patterns with two integer ops per
-//     pair (value * 2^-126, exact, subnormal for the 0.5 code), then one packed
-//     BF16 multiply by the block scale pre-multiplied by 2^118 (exact); the
-//     final 2^8 and the global scale g meet the FP32 sum in the epilogue;
-//   * the K order inside each 128-element chunk is permuted so that a lane's
-//     16-byte load feeds its A fragments directly; the activations are laid out
-//     once per CTA in shared memory in the same permuted fragment order (one
-//     conflict-free 8-byte load per MMA), normalised on the way in;
-//   * split-K inside the CTA (ks warps per 16-row tile) for small n, reduced in
-//     a fixed order through shared memory (deterministic, so equal rows give
-//     bit-equal logits);
-//   * argmax: a 64-bit key (order-preserving float bits, inverted index) per
+// weight incl. scales) from HBM.
+//   * Weight stream: every warp owns a 4-stage shared-memory ring; one lane
+//     issues a 2-D TMA copy (cp.async.bulk.tensor, 16 rows x 64 bytes = one
+//     128-element K chunk of a 16-row tile) per stage with an mbarrier
+//     completion, so 4 KB per warp are in flight without holding registers.
+//     Rows past n and bytes past k/2 arrive as zeros (TMA bounds fill), which
+//     removes every predicate from the loop.  Block scales (2 bytes per lane and
+//     row) are prefetched into registers as far ahead as the ring.
+//   * Products on the tensor cores: warp-level mma.sync m16n8k16 (FP16 in,
+//     FP32 accumulate).  A = the 16-row weight tile: each E2M1 pair becomes an
+//     exact f16x2 by the hardware conversion, times the block scale (E4M3 ->
+//     F16, exact; the product has at most 6 significant bits).  B = the (up to
+//     8) activation rows, FP16 after an exact per-row power-of-two scale that
+//     the epilogue removes.  On CUDA cores an 8-row batch would need 8 FP32
+//     FMAs per weight on top of the dequantisation; here the instruction count
+//     per weight does not depend on m.
+//   * Lane (g, t) of a warp reads rows g and g+8, K elements 32t..32t+31 of the
+//     chunk; MMA 2w+u takes elements 32t+8w+4u .. +3, so one B fragment is four
+//     consecutive activations, laid out once per CTA in shared memory in that
+//     order (one conflict-free 8-byte load per MMA), normalised on the way in.
+//   * Split K inside the CTA (ks warps per 16-row tile) for small n; partials
+//     are combined in a fixed order (deterministic: equal weight rows give
+//     bit-equal logits).
+//   * Argmax: a 64-bit key (order-preserving float bits, inverted index) per
 //     row, max-reduced per lane, warp, CTA, then one atomicMax per CTA; the last
 //     CTA to finish converts the keys and returns the workspace to zero.
+//   * Every mbarrier wait is bounded; one that runs out records
+//     NVFP4_ERR_TIMEOUT and the warp finishes its work without waiting again.
+#include <cuda.h>
 #include <cuda_fp8.h>
 
 #include "common.cuh"
 
 namespace {
 
-constexpr int kThreads = 512;
-constexpr int kWarps = kThreads / 32;
-constexpr int kChunk = 128;  // K elements per lane-group iteration (64 bytes per row)
-constexpr int kPF = 2;       // chunks in flight per lane (register double buffer)
+constexpr int kChunk = 128;       // K elements per chunk (64 packed bytes per row)
+constexpr int kRing = 4;          // TMA stages per warp
+constexpr int kStageBytes = 1024; // 16 rows x 64 bytes
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
 struct GemvParams {
   const __nv_bfloat16* x[2];
@@ -52,7 +57,6 @@ struct GemvParams {
   float eps[2];
   int nseg;
   int m;
-  const uint8_t* packed;
   const uint8_t* scales;
   const float* gscale;
   int64_t n, k;
@@ -66,15 +70,51 @@ struct GemvParams {
   int ks;          // warps sharing one 16-row tile (split K)
   int64_t ntiles;  // ceil(n / 16)
   int nchunks;     // ceil(k / 128)
-  int nfull;       // chunks lying entirely inside k (the rest is one tail chunk)
+  // shared-memory carve-up (bytes from the 1 KB-aligned base)
+  uint32_t off_red, off_small, off_kred, off_ring, off_bar;
 };
 
-__device__ __forceinline__ uint4 ld_stream_u4(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
+__device__ __forceinline__ unsigned long long globaltimer() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait; false (and NVFP4_ERR_TIMEOUT recorded) if it ran out.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int32_t* dev_status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer() - t0 > kWaitLimitNs) {
+      nvfp4::report(dev_status, NVFP4_ERR_TIMEOUT);
+      return false;
+    }
+  }
+  return true;
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+      : "memory");
 }
 
 __device__ __forceinline__ uint32_t f16x2_mul(uint32_t a, uint32_t b) {
@@ -162,9 +202,10 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // uint2 at bfrag[q * 4M + L].  For the 8 activations at
 // kk = 128 c + 32 t + 8 w (+0..7):  MMA 8c+2w gets {a0,a4},{a1,a5};
 // MMA 8c+2w+1 gets {a2,a6},{a3,a7}.  Positions past k are zero.
-template <int M>
+template <int M, int WARPS>
 __device__ void build_fragments(const GemvParams& p, uint2* bfrag, float* rms) {
   constexpr int BSTRIDE = 4 * M;
+  constexpr int kWarps = WARPS, kThreads = WARPS * 32;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   // 1. inverse RMS per (row, segment) job.  The CTA's warps split each job's
   //    k range (all 16 warps for a single job), four 16-byte loads in flight
@@ -296,78 +337,82 @@ __device__ __forceinline__ void bar_arrive(int id, int count) {
 }
 
 // ------------------------------------------------------------------ kernel
-// Work split: 16 warps per CTA; ks warps share one 16-row tile, each taking a
-// contiguous range of the k chunks (split K); a CTA takes 16/ks tiles at a
+// Work split: WARPS warps per CTA; ks warps share one 16-row tile, each taking
+// a contiguous range of its k chunks (split K); a CTA takes WARPS/ks tiles at a
 // time and strides over the tiles persistently.  Each warp streams its
-// (tile, chunk) items in order with PF items in flight, across tile
-// boundaries; the full chunks need no predicates (rows past n are clamped to
-// a valid row whose results are dropped).  A chunk reaching past k (only when
-// k % 128 != 0) is loaded with predicates at the end of each tile.
-template <int M>
-__global__ void __launch_bounds__(kThreads, 2)
-gemv_kernel(const __grid_constant__ GemvParams p) {
+// (tile, chunk) items in order through its TMA ring, across tile boundaries.
+template <int M, int WARPS>
+__global__ void __launch_bounds__(WARPS * 32, WARPS >= 16 ? 2 : 1)
+gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ GemvParams p) {
   constexpr int BSTRIDE = 4 * M;
-  extern __shared__ __align__(16) unsigned char smem[];
+  constexpr int kWarps = WARPS;
+  extern __shared__ unsigned char smem_raw[];
+  const uint32_t raw = static_cast<uint32_t>(__cvta_generic_to_shared(smem_raw));
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  unsigned char* const smem = smem_raw + (base - raw);
   uint2* bfrag = reinterpret_cast<uint2*>(smem);
-  const size_t bbytes = (size_t)p.nchunks * 8 * BSTRIDE * sizeof(uint2);
-  float* red = reinterpret_cast<float*>(smem + bbytes);                // [2][kWarps][32][4]
-  float* rms = red + 2 * kWarps * 32 * 4;                    // [16] + partial sums [16][kWarps]
-  // after rms: partial sums [16][kWarps], row maxima [8], row scales [16]
-  unsigned long long* kred =
-      reinterpret_cast<unsigned long long*>(rms + 16 + 16 * kWarps + 8 + 16);  // [kWarps][32][2]
+  float* red = reinterpret_cast<float*>(smem + p.off_red);  // [kWarps][32][4]
+  float* rms = reinterpret_cast<float*>(smem + p.off_small);
+  unsigned long long* kred = reinterpret_cast<unsigned long long*>(smem + p.off_kred);
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, t = lane & 3;
   const int ks = p.ks;
   const int tpc = kWarps / ks;  // tiles per CTA iteration
   const int slot = warp / ks, kpart = warp % ks;
-  // this warp's full chunks [cb, cb + L)
-  const int cb = (int)((int64_t)kpart * p.nfull / ks);
-  const int L = (int)((int64_t)(kpart + 1) * p.nfull / ks) - cb;
-  const bool tail = p.nfull < p.nchunks && kpart == ks - 1;
+  // this warp's chunks [cb, cb + L) of every tile
+  const int cb = (int)((int64_t)kpart * p.nchunks / ks);
+  const int L = (int)((int64_t)(kpart + 1) * p.nchunks / ks) - cb;
   const int64_t ngroups = (p.ntiles + tpc - 1) / tpc;
   const int n_iter = blockIdx.x < ngroups ? (int)((ngroups - 1 - blockIdx.x) / gridDim.x) + 1 : 0;
-  const int64_t rowbytes = p.k / 2, rowscales = p.k / 16;
+  const int64_t rowscales = p.k / 16;
+  const uint32_t ring = base + p.off_ring + (uint32_t)warp * (kRing * kStageBytes);
+  const uint32_t bars = base + p.off_bar + (uint32_t)warp * (kRing * 8);
+  bool alive = true;  // false once a wait ran out
 
-  // load cursor: item (lt, lc) -> byte offsets of tile lt's two rows, chunk lc
-  // (32-bit offsets: the host rejects weights of 4 GiB or more)
+  if (lane == 0) {
+    for (int i = 0; i < kRing; ++i) mbar_init(bars + 8 * i, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncwarp();
+
+  // load cursor over (tile, chunk)
   int lt = 0, lc = 0;
-  uint32_t lo0 = 0, lo1 = 0;  // packed offsets of rows g, g + 8 at chunk cb
+  int64_t lrow0 = 0, lrow1 = 0, ltile = 0;
   auto set_tile = [&](int it) {
-    const int64_t tile = ((int64_t)blockIdx.x + (int64_t)it * gridDim.x) * tpc + slot;
-    int64_t r0 = tile * 16 + g, r1 = r0 + 8;
-    r0 = r0 < p.n ? r0 : p.n - 1;
-    r1 = r1 < p.n ? r1 : p.n - 1;
-    lo0 = (uint32_t)(r0 * rowbytes + 16 * t + (int64_t)cb * 64);
-    lo1 = (uint32_t)(r1 * rowbytes + 16 * t + (int64_t)cb * 64);
+    ltile = ((int64_t)blockIdx.x + (int64_t)it * gridDim.x) * tpc + slot;
+    lrow0 = ltile * 16 + g;
+    lrow1 = lrow0 + 8;
+    lrow0 = lrow0 < p.n ? lrow0 : p.n - 1;  // rows past n: any valid scale (codes are 0)
+    lrow1 = lrow1 < p.n ? lrow1 : p.n - 1;
   };
   const int total = n_iter * L;
-  uint4 qa[kPF], qb[kPF];
-  uint32_t sa[kPF], sb[kPF];
-  // The scale pair of a lane sits at byte (packed offset) / 8 of the scales:
-  // row r, chunk c, lane t -> packed byte r*k/2 + 64c + 16t, scale byte
-  // r*k/16 + 8c + 2t.
+  uint32_t sreg[kRing];  // block-scale pairs of rows g, g+8 (low / high 16 bits)
   auto issue = [&](int i) {
     if (lc == 0) set_tile(lt);
-    const uint32_t o0 = lo0 + (uint32_t)lc * 64, o1 = lo1 + (uint32_t)lc * 64;
-    qa[i] = ld_stream_u4(p.packed + o0);
-    qb[i] = ld_stream_u4(p.packed + o1);
-    sa[i] = __ldg(reinterpret_cast<const uint16_t*>(p.scales + (o0 >> 3)));
-    sb[i] = __ldg(reinterpret_cast<const uint16_t*>(p.scales + (o1 >> 3)));
+    const int c = cb + lc;
+    if (lane == 0) {
+      mbar_arrive_expect_tx(bars + 8 * i, kStageBytes);
+      tma_load_2d(ring + i * kStageBytes, &tmap_w, c * 64, (int)(ltile * 16), bars + 8 * i);
+    }
+    const bool kv = (int64_t)c * kChunk + 32 * t < p.k;
+    const uint16_t* s0 = reinterpret_cast<const uint16_t*>(p.scales + lrow0 * rowscales) + t + 4 * c;
+    const uint16_t* s1 = reinterpret_cast<const uint16_t*>(p.scales + lrow1 * rowscales) + t + 4 * c;
+    sreg[i] = kv ? ((uint32_t)__ldg(s0) | ((uint32_t)__ldg(s1) << 16)) : 0u;
     if (++lc == L) { lc = 0; ++lt; }
   };
   // start streaming before the activation prologue
 #pragma unroll
-  for (int i = 0; i < kPF; ++i)
+  for (int i = 0; i < kRing; ++i)
     if (i < total) issue(i);
 
-  if (n_iter > 0 || blockIdx.x == 0) build_fragments<M>(p, bfrag, rms);
+  if (n_iter > 0 || blockIdx.x == 0) build_fragments<M, WARPS>(p, bfrag, rms);
   __syncthreads();
 
   const float gsc = __ldg(p.gscale);
   // inverse activation scales of this lane's two batch columns (2t, 2t+1)
-  const float* rowscale = reinterpret_cast<const float*>(
-      reinterpret_cast<const unsigned int*>(rms + 16 + 16 * kWarps) + 8);
+  const float* rowscale =
+      reinterpret_cast<const float*>(reinterpret_cast<const unsigned int*>(rms + 16 + 16 * kWarps) + 8);
   const float inv0 = rowscale[8 + min(2 * t, M - 1)], inv1 = rowscale[8 + min(2 * t + 1, M - 1)];
   const uint2* bbase = bfrag + (lane % BSTRIDE);
   // running argmax keys of this lane's two batch columns live in shared memory
@@ -379,36 +424,19 @@ gemv_kernel(const __grid_constant__ GemvParams p) {
 
   auto epilogue = [&](int it) {
     const int64_t tile = ((int64_t)blockIdx.x + (int64_t)it * gridDim.x) * tpc + slot;
-    if (tail) {  // the chunk reaching past k, with predicates
-      const int c = p.nfull;
-      const bool kv = (int64_t)c * kChunk + 32 * t < p.k;
-      int64_t r0 = tile * 16 + g, r1 = r0 + 8;
-      r0 = r0 < p.n ? r0 : p.n - 1;
-      r1 = r1 < p.n ? r1 : p.n - 1;
-      uint4 q0 = make_uint4(0, 0, 0, 0), q1 = make_uint4(0, 0, 0, 0);
-      uint32_t s0 = 0, s1 = 0;
-      if (kv && tile < p.ntiles) {
-        q0 = ld_stream_u4(p.packed + r0 * rowbytes + 16 * t + (int64_t)c * 64);
-        q1 = ld_stream_u4(p.packed + r1 * rowbytes + 16 * t + (int64_t)c * 64);
-        s0 = __ldg(reinterpret_cast<const uint16_t*>(p.scales + r0 * rowscales) + t + 4 * c);
-        s1 = __ldg(reinterpret_cast<const uint16_t*>(p.scales + r1 * rowscales) + t + 4 * c);
-      }
-      chunk_mma<BSTRIDE>(acc, q0, q1, s0, s1, bbase + (int64_t)(8 * c) * BSTRIDE);
-    }
     if (ks > 1) {
-      float* rb = red + (size_t)(it & 1) * kWarps * 32 * 4;
       const int full_id = 1 + slot, empty_id = 5 + slot;  // slot < 4 when ks >= 4
+      float* mine = red + (warp * 32 + lane) * 4;
       if (kpart != 0) {
-        // The consumer has finished tile it-1 (so no producer can arrive on the
-        // full barrier twice before it completes).
+        // the consumer has finished tile it-1 (so no producer can arrive on the
+        // full barrier twice before it completes, and the buffer is free)
         if (it >= 1) bar_sync(empty_id, ks * 32);
-        float* mine = rb + (warp * 32 + lane) * 4;
         mine[0] = acc[0]; mine[1] = acc[1]; mine[2] = acc[2]; mine[3] = acc[3];
         bar_arrive(full_id, ks * 32);
       } else {
         bar_sync(full_id, ks * 32);
         for (int j = 1; j < ks; ++j) {
-          const float* o = rb + ((warp + j) * 32 + lane) * 4;
+          const float* o = red + ((warp + j) * 32 + lane) * 4;
           acc[0] += o[0]; acc[1] += o[1]; acc[2] += o[2]; acc[3] += o[3];
         }
         bar_arrive(empty_id, ks * 32);
@@ -441,31 +469,35 @@ gemv_kernel(const __grid_constant__ GemvParams p) {
     acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
   };
 
-  if (L == 0) {
-    for (int it = 0; it < n_iter; ++it) epilogue(it);
-  } else {
-    for (int q = 0; q < total; q += kPF) {
+  for (int q0 = 0; q0 < total; q0 += kRing) {
 #pragma unroll
-      for (int i = 0; i < kPF; ++i) {
-        if (q + i < total) {
-          chunk_mma<BSTRIDE>(acc, qa[i], qb[i], sa[i], sb[i],
-                             bbase + (int64_t)(8 * (cb + cc)) * BSTRIDE);
-          if (q + i + kPF < total) issue(i);
-          if (++cc == L) {
-            epilogue(ct);
-            cc = 0;
-            ++ct;
-          }
+    for (int i = 0; i < kRing; ++i) {
+      const int q = q0 + i;
+      if (q < total) {
+        if (alive) alive = mbar_wait(bars + 8 * i, (uint32_t)(q / kRing) & 1u, p.dev_status);
+        const unsigned char* st = smem + (ring - base) + i * kStageBytes;
+        const uint4 qg = *reinterpret_cast<const uint4*>(st + g * 64 + t * 16);
+        const uint4 qh = *reinterpret_cast<const uint4*>(st + (g + 8) * 64 + t * 16);
+        const uint32_t s2 = sreg[i];
+        chunk_mma<BSTRIDE>(acc, qg, qh, s2 & 0xFFFFu, s2 >> 16,
+                           bbase + (int64_t)(8 * (cb + cc)) * BSTRIDE);
+        __syncwarp();  // every lane is done with stage i before it is refilled
+        if (q + kRing < total) issue(i);
+        if (++cc == L) {
+          epilogue(ct);
+          cc = 0;
+          ++ct;
         }
       }
     }
   }
+  if (L == 0)  // no chunk for this warp: still take part in every tile's epilogue
+    for (int it = 0; it < n_iter; ++it) epilogue(it);
 
   if (ks > 1 && kpart != 0 && n_iter > 0)  // match the consumer's last "empty" arrival
     bar_sync(5 + slot, ks * 32);
 
   if (p.keys == nullptr) return;
-  // argmax: lanes sharing t hold the same two rows of the batch
   __syncthreads();
   if (threadIdx.x < (unsigned)M) {
     // column m is held by the lanes with t = m / 2, slot m % 2, of every warp
@@ -494,19 +526,44 @@ gemv_kernel(const __grid_constant__ GemvParams p) {
   }
 }
 
-using KernelFn = void (*)(GemvParams);
+using KernelFn = void (*)(CUtensorMap, GemvParams);
 
+template <int WARPS>
 KernelFn kernel_for(int m) {
   switch (m) {
-    case 1: return gemv_kernel<1>;
-    case 2: return gemv_kernel<2>;
-    case 3: return gemv_kernel<3>;
-    case 4: return gemv_kernel<4>;
-    case 5: return gemv_kernel<5>;
-    case 6: return gemv_kernel<6>;
-    case 7: return gemv_kernel<7>;
-    default: return gemv_kernel<8>;
+    case 1: return gemv_kernel<1, WARPS>;
+    case 2: return gemv_kernel<2, WARPS>;
+    case 3: return gemv_kernel<3, WARPS>;
+    case 4: return gemv_kernel<4, WARPS>;
+    case 5: return gemv_kernel<5, WARPS>;
+    case 6: return gemv_kernel<6, WARPS>;
+    case 7: return gemv_kernel<7, WARPS>;
+    default: return gemv_kernel<8, WARPS>;
   }
+}
+
+struct Layout {
+  uint32_t off_red, off_small, off_kred, off_ring, off_bar;
+  size_t bytes;  // dynamic shared memory to request (includes 1 KB alignment slack)
+};
+
+Layout layout_for(int warps, int m, int nchunks) {
+  Layout l;
+  size_t off = (size_t)nchunks * 8 * 4 * m * sizeof(uint2);  // B fragments
+  l.off_red = (uint32_t)off;
+  off += (size_t)warps * 32 * 4 * sizeof(float);
+  l.off_small = (uint32_t)off;
+  off += (16 + 16 * warps + 8 + 16) * sizeof(float);
+  off = (off + 15) & ~(size_t)15;
+  l.off_kred = (uint32_t)off;
+  off += (size_t)warps * 32 * 2 * sizeof(unsigned long long);
+  off = (off + 1023) & ~(size_t)1023;
+  l.off_ring = (uint32_t)off;
+  off += (size_t)warps * kRing * kStageBytes;
+  l.off_bar = (uint32_t)off;
+  off += (size_t)warps * kRing * 8;
+  l.bytes = off + 1024;
+  return l;
 }
 
 }  // namespace
@@ -524,7 +581,6 @@ int launch_gemv(const w4a16_act_segment* seg, int nseg, int m, const nvfp4_weigh
   }
   p.nseg = nseg;
   p.m = m;
-  p.packed = w->packed;
   p.scales = w->scales;
   p.gscale = w->global_scale;
   p.n = w->n;
@@ -540,26 +596,48 @@ int launch_gemv(const w4a16_act_segment* seg, int nseg, int m, const nvfp4_weigh
   p.dev_status = dev_status;
   p.ntiles = nvfp4::cdiv(w->n, 16);
   p.nchunks = (int)nvfp4::cdiv(w->k, kChunk);
-  p.nfull = (int)(w->k / kChunk);
+  if (p.ntiles * 16 > 0x7FFFFFFFLL) return NVFP4_ERR_SHAPE;  // TMA row coordinate
 
-  const size_t bbytes = (size_t)p.nchunks * 8 * 4 * m * sizeof(uint2);
-  const size_t smem = bbytes + 2 * kWarps * 32 * 4 * sizeof(float) +
-                      (16 + 16 * kWarps + 8 + 16) * sizeof(float) +
-                      kWarps * 32 * 2 * sizeof(unsigned long long);
-  KernelFn fn = kernel_for(m);
-  const int occ = nvfp4::occupancy(reinterpret_cast<const void*>(fn), kThreads, smem);
+  // 16-warp CTAs when their shared memory fits, else 8-warp CTAs.
+  int warps = 16;
+  Layout lay = layout_for(16, m, p.nchunks);
+  KernelFn fn = kernel_for<16>(m);
+  int occ = nvfp4::occupancy(reinterpret_cast<const void*>(fn), 16 * 32, lay.bytes);
+  if (occ < 1) {
+    warps = 8;
+    lay = layout_for(8, m, p.nchunks);
+    fn = kernel_for<8>(m);
+    occ = nvfp4::occupancy(reinterpret_cast<const void*>(fn), 8 * 32, lay.bytes);
+  }
   if (occ < 1) return NVFP4_ERR_CUDA;
+  p.off_red = lay.off_red;
+  p.off_small = lay.off_small;
+  p.off_kred = lay.off_kred;
+  p.off_ring = lay.off_ring;
+  p.off_bar = lay.off_bar;
+
+  CUtensorMap tmap;
+  const cuuint64_t dims[2] = {(cuuint64_t)(w->k / 2), (cuuint64_t)w->n};
+  const cuuint64_t strides[1] = {(cuuint64_t)(w->k / 2)};
+  const cuuint32_t box[2] = {64, 16};
+  const cuuint32_t estr[2] = {1, 1};
+  if (!nvfp4::encode_tiled(&tmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(w->packed),
+                           dims, strides, box, estr, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return NVFP4_ERR_CUDA;
+
   const int sms = nvfp4::sm_count();
   const int64_t slots = (int64_t)sms * occ;  // resident CTAs
   // Split K (ks warps per tile) until the resident CTAs each get several tile
-  // groups to stream, keeping at least 4 full chunks per warp.
+  // groups to stream, keeping at least 4 chunks per warp; split factors are 1,
+  // 4, 8, 16 (at most 4 tile groups per CTA share its named barriers).
   int ks = 1;
-  while (ks < kWarps && nvfp4::cdiv(p.ntiles, kWarps / ks) < 4 * slots && p.nfull / (2 * ks) >= 4)
+  while (ks < warps && nvfp4::cdiv(p.ntiles, warps / ks) < 4 * slots && p.nchunks / (2 * ks) >= 4)
     ks = ks == 1 ? 4 : 2 * ks;
+  if (ks > 1 && warps / ks > 4) ks = warps / 4;
   p.ks = ks;
-  const int64_t ngroups = nvfp4::cdiv(p.ntiles, kWarps / ks);
+  const int64_t ngroups = nvfp4::cdiv(p.ntiles, warps / ks);
   const int64_t grid = ngroups < slots ? ngroups : slots;
-  fn<<<(unsigned)grid, kThreads, smem, stream>>>(p);
+  fn<<<(unsigned)grid, warps * 32, lay.bytes, stream>>>(tmap, p);
   if (cudaGetLastError() != cudaSuccess) return NVFP4_ERR_CUDA;
   return NVFP4_OK;
 }
