@@ -45,8 +45,9 @@
 namespace {
 
 constexpr int kChunk = 128;       // K elements per chunk (64 packed bytes per row)
-constexpr int kRing = 4;          // TMA stages per warp
-constexpr int kStageBytes = 1024; // 16 rows x 64 bytes
+constexpr int kRing = 2;          // TMA stages per warp
+constexpr int kItem = 2;          // chunks per stage (one TMA box of 16 rows x 128 bytes)
+constexpr int kStageBytes = 16 * 64 * kItem;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
 struct GemvParams {
@@ -360,14 +361,16 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
   const int ks = p.ks;
   const int tpc = kWarps / ks;  // tiles per CTA iteration
   const int slot = warp / ks, kpart = warp % ks;
-  // this warp's chunks [cb, cb + L) of every tile
-  const int cb = (int)((int64_t)kpart * p.nchunks / ks);
-  const int L = (int)((int64_t)(kpart + 1) * p.nchunks / ks) - cb;
+  // this warp's items (pairs of chunks) [ib, ib + L) of every tile
+  const int nitems = (p.nchunks + kItem - 1) / kItem;
+  const int ib = (int)((int64_t)kpart * nitems / ks);
+  const int L = (int)((int64_t)(kpart + 1) * nitems / ks) - ib;
   const int64_t ngroups = (p.ntiles + tpc - 1) / tpc;
   const int n_iter = blockIdx.x < ngroups ? (int)((ngroups - 1 - blockIdx.x) / gridDim.x) + 1 : 0;
-  const int64_t rowscales = p.k / 16;
   const uint32_t ring = base + p.off_ring + (uint32_t)warp * (kRing * kStageBytes);
   const uint32_t bars = base + p.off_bar + (uint32_t)warp * (kRing * 8);
+  // chunks c with 128c + 32t < k hold this lane's data (scales past k read 0)
+  const int cmax = (int)((p.k - 32 * t + kChunk - 1) / kChunk);
   bool alive = true;  // false once a wait ran out
 
   if (lane == 0) {
@@ -376,30 +379,38 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
   }
   __syncwarp();
 
-  // load cursor over (tile, chunk)
+  // load cursor over (tile, item); scale row pointers change once per tile
   int lt = 0, lc = 0;
-  int64_t lrow0 = 0, lrow1 = 0, ltile = 0;
+  int ltile16 = 0;
+  const uint16_t* sp0 = nullptr;
+  const uint16_t* sp1 = nullptr;
   auto set_tile = [&](int it) {
-    ltile = ((int64_t)blockIdx.x + (int64_t)it * gridDim.x) * tpc + slot;
-    lrow0 = ltile * 16 + g;
-    lrow1 = lrow0 + 8;
-    lrow0 = lrow0 < p.n ? lrow0 : p.n - 1;  // rows past n: any valid scale (codes are 0)
-    lrow1 = lrow1 < p.n ? lrow1 : p.n - 1;
+    const int64_t tile = ((int64_t)blockIdx.x + (int64_t)it * gridDim.x) * tpc + slot;
+    ltile16 = (int)(tile * 16);
+    int64_t r0 = tile * 16 + g, r1 = r0 + 8;
+    r0 = r0 < p.n ? r0 : p.n - 1;  // rows past n: any valid scale (their codes read as 0)
+    r1 = r1 < p.n ? r1 : p.n - 1;
+    sp0 = reinterpret_cast<const uint16_t*>(p.scales + r0 * (p.k / 16)) + t;
+    sp1 = reinterpret_cast<const uint16_t*>(p.scales + r1 * (p.k / 16)) + t;
   };
   const int total = n_iter * L;
-  uint32_t sreg[kRing];  // block-scale pairs of rows g, g+8 (low / high 16 bits)
+  uint32_t sreg[kRing][kItem];  // block-scale pairs of rows g, g+8 (low / high 16 bits)
+  if (total > 0) set_tile(0);
   auto issue = [&](int i) {
-    if (lc == 0) set_tile(lt);
-    const int c = cb + lc;
+    const int c0 = (ib + lc) * kItem;
     if (lane == 0) {
       mbar_arrive_expect_tx(bars + 8 * i, kStageBytes);
-      tma_load_2d(ring + i * kStageBytes, &tmap_w, c * 64, (int)(ltile * 16), bars + 8 * i);
+      tma_load_2d(ring + i * kStageBytes, &tmap_w, c0 * 64, ltile16, bars + 8 * i);
     }
-    const bool kv = (int64_t)c * kChunk + 32 * t < p.k;
-    const uint16_t* s0 = reinterpret_cast<const uint16_t*>(p.scales + lrow0 * rowscales) + t + 4 * c;
-    const uint16_t* s1 = reinterpret_cast<const uint16_t*>(p.scales + lrow1 * rowscales) + t + 4 * c;
-    sreg[i] = kv ? ((uint32_t)__ldg(s0) | ((uint32_t)__ldg(s1) << 16)) : 0u;
-    if (++lc == L) { lc = 0; ++lt; }
+#pragma unroll
+    for (int j = 0; j < kItem; ++j) {
+      const int c = c0 + j;
+      sreg[i][j] = c < cmax ? ((uint32_t)__ldg(sp0 + 4 * c) | ((uint32_t)__ldg(sp1 + 4 * c) << 16)) : 0u;
+    }
+    if (++lc == L) {
+      lc = 0;
+      if (++lt < n_iter) set_tile(lt);
+    }
   };
   // start streaming before the activation prologue
 #pragma unroll
@@ -476,11 +487,15 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
       if (q < total) {
         if (alive) alive = mbar_wait(bars + 8 * i, (uint32_t)(q / kRing) & 1u, p.dev_status);
         const unsigned char* st = smem + (ring - base) + i * kStageBytes;
-        const uint4 qg = *reinterpret_cast<const uint4*>(st + g * 64 + t * 16);
-        const uint4 qh = *reinterpret_cast<const uint4*>(st + (g + 8) * 64 + t * 16);
-        const uint32_t s2 = sreg[i];
-        chunk_mma<BSTRIDE>(acc, qg, qh, s2 & 0xFFFFu, s2 >> 16,
-                           bbase + (int64_t)(8 * (cb + cc)) * BSTRIDE);
+        const uint2* bq = bbase + (int64_t)(8 * kItem * (ib + cc)) * BSTRIDE;
+#pragma unroll
+        for (int j = 0; j < kItem; ++j) {  // box rows are 64 * kItem bytes
+          const uint4 qg = *reinterpret_cast<const uint4*>(st + g * (64 * kItem) + j * 64 + t * 16);
+          const uint4 qh =
+              *reinterpret_cast<const uint4*>(st + (g + 8) * (64 * kItem) + j * 64 + t * 16);
+          const uint32_t s2 = sreg[i][j];
+          chunk_mma<BSTRIDE>(acc, qg, qh, s2 & 0xFFFFu, s2 >> 16, bq + 8 * j * BSTRIDE);
+        }
         __syncwarp();  // every lane is done with stage i before it is refilled
         if (q + kRing < total) issue(i);
         if (++cc == L) {
@@ -595,7 +610,9 @@ int launch_gemv(const w4a16_act_segment* seg, int nseg, int m, const nvfp4_weigh
   }
   p.dev_status = dev_status;
   p.ntiles = nvfp4::cdiv(w->n, 16);
-  p.nchunks = (int)nvfp4::cdiv(w->k, kChunk);
+  // round k's chunks up to whole items: the padding chunk's activations are
+  // zero and its weights arrive as zeros (TMA bounds fill)
+  p.nchunks = (int)(nvfp4::cdiv(nvfp4::cdiv(w->k, kChunk), kItem) * kItem);
   if (p.ntiles * 16 > 0x7FFFFFFFLL) return NVFP4_ERR_SHAPE;  // TMA row coordinate
 
   // 16-warp CTAs when their shared memory fits, else 8-warp CTAs.
@@ -619,7 +636,7 @@ int launch_gemv(const w4a16_act_segment* seg, int nseg, int m, const nvfp4_weigh
   CUtensorMap tmap;
   const cuuint64_t dims[2] = {(cuuint64_t)(w->k / 2), (cuuint64_t)w->n};
   const cuuint64_t strides[1] = {(cuuint64_t)(w->k / 2)};
-  const cuuint32_t box[2] = {64, 16};
+  const cuuint32_t box[2] = {64 * kItem, 16};
   const cuuint32_t estr[2] = {1, 1};
   if (!nvfp4::encode_tiled(&tmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(w->packed),
                            dims, strides, box, estr, CU_TENSOR_MAP_SWIZZLE_NONE))
@@ -631,7 +648,8 @@ int launch_gemv(const w4a16_act_segment* seg, int nseg, int m, const nvfp4_weigh
   // groups to stream, keeping at least 4 chunks per warp; split factors are 1,
   // 4, 8, 16 (at most 4 tile groups per CTA share its named barriers).
   int ks = 1;
-  while (ks < warps && nvfp4::cdiv(p.ntiles, warps / ks) < 4 * slots && p.nchunks / (2 * ks) >= 4)
+  while (ks < warps && nvfp4::cdiv(p.ntiles, warps / ks) < 4 * slots &&
+         p.nchunks / kItem / (2 * ks) >= 2)
     ks = ks == 1 ? 4 : 2 * ks;
   if (ks > 1 && warps / ks > 4) ks = warps / 4;
   p.ks = ks;
