@@ -49,6 +49,7 @@ constexpr int kRing = 2;          // TMA stages per warp
 constexpr int kItem = 2;          // chunks per stage (one TMA box of 16 rows x 128 bytes)
 constexpr int kStageBytes = 16 * 64 * kItem;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+constexpr int kL2Prefetch = 8;    // items per warp pulled into L2 while the previous call ends
 
 struct GemvParams {
   const __nv_bfloat16* x[2];
@@ -412,6 +413,25 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
       if (++lt < n_iter) set_tile(lt);
     }
   };
+  // Back-to-back calls (programmatic dependent launch): let the next grid
+  // start now, pull this warp's first weight boxes into L2 (a hint only: L2 is
+  // the point of coherence, so this is correct even if the previous kernel on
+  // the stream is still writing them), then wait for the previous grid to
+  // finish before reading anything.  Without PDL both controls are no-ops.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (lane == 0) {
+    int pt = 0, pc = 0;
+    for (int q = 0; q < total && q < kL2Prefetch; ++q) {
+      const int64_t tile = ((int64_t)blockIdx.x + (int64_t)pt * gridDim.x) * tpc + slot;
+      asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global [%0, {%1, %2}];" ::"l"(
+                       reinterpret_cast<uint64_t>(&tmap_w)),
+                   "r"((ib + pc) * kItem * 64), "r"((int)(tile * 16))
+                   : "memory");
+      if (++pc == L) { pc = 0; ++pt; }
+    }
+  }
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+
   // start streaming before the activation prologue
 #pragma unroll
   for (int i = 0; i < kRing; ++i)
@@ -654,8 +674,23 @@ int launch_gemv(const w4a16_act_segment* seg, int nseg, int m, const nvfp4_weigh
   if (ks > 1 && warps / ks > 4) ks = warps / 4;
   p.ks = ks;
   const int64_t ngroups = nvfp4::cdiv(p.ntiles, warps / ks);
-  const int64_t grid = ngroups < slots ? ngroups : slots;
-  fn<<<(unsigned)grid, warps * 32, lay.bytes, stream>>>(tmap, p);
+  // Calls small enough to be dominated by their fixed costs use one CTA per SM
+  // so the next call's CTAs (launched programmatically, see the kernel) can
+  // share the SM and prefetch while this one finishes.
+  const int64_t wbytes = w->n * (w->k / 2 + w->k / 16);
+  const int64_t cap = (occ > 1 && wbytes < ((int64_t)256 << 20)) ? sms : slots;
+  const int64_t grid = ngroups < cap ? ngroups : cap;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(warps * 32);
+  cfg.dynamicSmemBytes = lay.bytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, fn, tmap, p) != cudaSuccess) return NVFP4_ERR_CUDA;
   if (cudaGetLastError() != cudaSuccess) return NVFP4_ERR_CUDA;
   return NVFP4_OK;
 }
