@@ -198,6 +198,16 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// 2^e (or 2^-e when inverse) for a row whose largest BF16 magnitude has the
+// bit pattern `maxbits`: e = 14 - exponent(max), clamped to [-120, 120]; 1 for
+// an all-zero row.
+__device__ __forceinline__ float row_scale_pow2(unsigned int maxbits, bool inverse) {
+  const int ef = (int)(maxbits >> 7);  // biased BF16 exponent
+  int e = maxbits == 0u ? 0 : 14 - (ef == 0 ? -126 : ef - 127);
+  e = e < -120 ? -120 : (e > 120 ? 120 : e);
+  return ldexpf(1.0f, inverse ? -e : e);
+}
+
 // ---------------------------------------------------------------- prologue
 // Normalise (optionally) and lay out the activations as B fragments.
 // Fragment layout: MMA index q = 8 * chunk + j, lane L = 4 * m + t (m < M):
@@ -214,6 +224,8 @@ __device__ void build_fragments(const GemvParams& p, uint2* bfrag, float* rms) {
   //    per lane; per-(job, warp) partial sums are combined in a fixed order,
   //    so the result does not depend on timing.
   float* part = rms + 16;  // [16 jobs][kWarps]
+  unsigned int* rowmax = reinterpret_cast<unsigned int*>(part + 16 * kWarps);  // [8]
+  if (tid < 8) rowmax[tid] = 0u;  // ordered before its use by the barriers below
   const int J = M * p.nseg;
   const int wpj = J >= kWarps ? 1 : kWarps / J;  // warps per job
   const int jpp = kWarps / wpj;                  // jobs per pass
@@ -255,10 +267,6 @@ __device__ void build_fragments(const GemvParams& p, uint2* bfrag, float* rms) {
   //    8c+2w+1 (elements 4..7) of lane 4m + t.  Positions past k are zero.
   //    The largest magnitude of each row is collected on the way (the BF16
   //    magnitude bits order like the values).
-  unsigned int* rowmax = reinterpret_cast<unsigned int*>(part + 16 * kWarps);  // [8]
-  float* rowscale = reinterpret_cast<float*>(rowmax + 8);                        // [8]
-  if (tid < 8) rowmax[tid] = 0u;
-  __syncthreads();
   const int64_t gpr = (int64_t)p.nchunks * (kChunk / 8);  // 8-element groups per row
 #pragma unroll 4
   for (int64_t gi = tid; gi < (int64_t)M * gpr; gi += kThreads) {
@@ -296,21 +304,12 @@ __device__ void build_fragments(const GemvParams& p, uint2* bfrag, float* rms) {
     bfrag[(int64_t)(8 * c + 2 * w + 1) * BSTRIDE + L] = make_uint2(a[2], a[3]);
   }
   __syncthreads();
-  // 3. per-row power-of-two scale 2^e so that max |a| * 2^e lies in [2^14, 2^15):
-  //    every BF16 activation within 2^-31 of the row's largest magnitude then
-  //    converts to FP16 exactly (8 significant bits, FP16 normal range).
-  if (tid < M) {
-    const int ef = (int)(rowmax[tid] >> 7);  // biased BF16 exponent of the row maximum
-    int e = rowmax[tid] == 0u ? 0 : 14 - (ef == 0 ? -126 : ef - 127);
-    e = e < -120 ? -120 : (e > 120 ? 120 : e);
-    rowscale[tid] = ldexpf(1.0f, e);
-    rowscale[8 + tid] = ldexpf(1.0f, -e);  // undone on the FP32 sum
-  }
-  __syncthreads();
-  // 4. BF16 -> scaled FP16 in place
+  // 3. BF16 -> FP16 in place, times a per-row power of two 2^e that puts the
+  //    row's largest magnitude in [2^14, 2^15): every BF16 activation within
+  //    2^-31 of it then converts exactly (8 significant bits, FP16 normal range).
   const int64_t slots = (int64_t)p.nchunks * 8 * BSTRIDE;
   for (int64_t i = tid; i < slots; i += kThreads) {
-    const float sc = rowscale[(int)(i % BSTRIDE) / 4];
+    const float sc = row_scale_pow2(rowmax[(int)(i % BSTRIDE) / 4], false);
     uint2 v = bfrag[i];
     const uint32_t u[2] = {v.x, v.y};
     uint32_t o[2];
@@ -442,9 +441,9 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
 
   const float gsc = __ldg(p.gscale);
   // inverse activation scales of this lane's two batch columns (2t, 2t+1)
-  const float* rowscale =
-      reinterpret_cast<const float*>(reinterpret_cast<const unsigned int*>(rms + 16 + 16 * kWarps) + 8);
-  const float inv0 = rowscale[8 + min(2 * t, M - 1)], inv1 = rowscale[8 + min(2 * t + 1, M - 1)];
+  const unsigned int* rowmax = reinterpret_cast<const unsigned int*>(rms + 16 + 16 * kWarps);
+  const float inv0 = row_scale_pow2(rowmax[min(2 * t, M - 1)], true);
+  const float inv1 = row_scale_pow2(rowmax[min(2 * t + 1, M - 1)], true);
   const uint2* bbase = bfrag + (lane % BSTRIDE);
   // running argmax keys of this lane's two batch columns live in shared memory
   unsigned long long* best = kred + (warp * 32 + lane) * 2;
@@ -543,21 +542,30 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
         const unsigned long long o = kred[(w * 32 + gg * 4 + m / 2) * 2 + (m & 1)];
         b = o > b ? o : b;
       }
-    if (b != 0ull) atomicMax(p.keys + m, b);
+    if (b != 0ull)
+      asm volatile("red.relaxed.gpu.global.max.u64 [%0], %1;" ::"l"(p.keys + m), "l"(b) : "memory");
   }
-  __threadfence();
+  // Count the finished CTAs with an acquire-release add: the barrier orders this
+  // CTA's key updates before thread 0's release, and the last CTA's acquire
+  // makes every CTA's keys visible to it, without separate fences.
   __syncthreads();
-  __shared__ bool last;
-  if (threadIdx.x == 0) last = atomicAdd(p.counter, 1u) == gridDim.x - 1;
+  __shared__ unsigned int prev;
+  if (threadIdx.x == 0) {
+    unsigned int v;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(v) : "l"(p.counter) : "memory");
+    prev = v;
+  }
   __syncthreads();
-  if (last) {
-    __threadfence();
+  if (prev == gridDim.x - 1) {  // the last CTA: convert the keys and re-zero the workspace
     if (threadIdx.x < (unsigned)M) {
-      const unsigned long long key = atomicExch(p.keys + threadIdx.x, 0ull);
+      unsigned long long key;
+      asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(key) : "l"(p.keys + threadIdx.x) : "memory");
+      asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p.keys + threadIdx.x), "l"(0ull) : "memory");
       p.argmax[threadIdx.x] =
           key == 0ull ? 0 : (int32_t)(0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFull));
     }
-    if (threadIdx.x == 0) atomicExch(p.counter, 0u);
+    if (threadIdx.x == 0)
+      asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p.counter), "r"(0u) : "memory");
   }
 }
 
