@@ -682,12 +682,7 @@ int launch_gemv(const w4a16_act_segment* seg, int nseg, int m, const nvfp4_weigh
   if (ks > 1 && warps / ks > 4) ks = warps / 4;
   p.ks = ks;
   const int64_t ngroups = nvfp4::cdiv(p.ntiles, warps / ks);
-  // Calls small enough to be dominated by their fixed costs use one CTA per SM
-  // so the next call's CTAs (launched programmatically, see the kernel) can
-  // share the SM and prefetch while this one finishes.
-  const int64_t wbytes = w->n * (w->k / 2 + w->k / 16);
-  const int64_t cap = (occ > 1 && wbytes < ((int64_t)256 << 20)) ? sms : slots;
-  const int64_t grid = ngroups < cap ? ngroups : cap;
+  const int64_t grid = ngroups < slots ? ngroups : slots;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
   cfg.blockDim = dim3(warps * 32);
