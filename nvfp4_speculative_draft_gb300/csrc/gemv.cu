@@ -45,9 +45,12 @@
 namespace {
 
 constexpr int kChunk = 128;       // K elements per chunk (64 packed bytes per row)
-constexpr int kRing = 2;          // TMA stages per warp
 constexpr int kItem = 2;          // chunks per stage (one TMA box of 16 rows x 128 bytes)
 constexpr int kStageBytes = 16 * 64 * kItem;
+// TMA stages per warp: batches of 4+ rows already hold one CTA per SM (their
+// staged activations are large), so they take a deeper ring; smaller batches
+// keep two CTAs per SM with two stages each.
+__host__ __device__ constexpr int ring_stages(int m, int warps) { return (warps >= 16 && m >= 4) ? 4 : 2; }
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 constexpr int kL2Prefetch = 8;    // items per warp pulled into L2 while the previous call ends
 
@@ -346,6 +349,7 @@ template <int M, int WARPS>
 __global__ void __launch_bounds__(WARPS * 32, WARPS >= 16 ? 2 : 1)
 gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ GemvParams p) {
   constexpr int BSTRIDE = 4 * M;
+  constexpr int kRing = ring_stages(M, WARPS);
   constexpr int kWarps = WARPS;
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = static_cast<uint32_t>(__cvta_generic_to_shared(smem_raw));
@@ -445,10 +449,7 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
   const float inv0 = row_scale_pow2(rowmax[min(2 * t, M - 1)], true);
   const float inv1 = row_scale_pow2(rowmax[min(2 * t + 1, M - 1)], true);
   const uint2* bbase = bfrag + (lane % BSTRIDE);
-  // running argmax keys of this lane's two batch columns live in shared memory
-  unsigned long long* best = kred + (warp * 32 + lane) * 2;
-  best[0] = 0ull;
-  best[1] = 0ull;
+  unsigned long long best[2] = {0ull, 0ull};  // running argmax keys, columns 2t and 2t+1
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
   int ct = 0, cc = 0;  // compute cursor
 
@@ -532,16 +533,27 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
     bar_sync(5 + slot, ks * 32);
 
   if (p.keys == nullptr) return;
+  // lanes sharing t hold the same two batch columns: reduce over g, then per warp
+#pragma unroll
+  for (int e = 0; e < 2; ++e) {
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+      const unsigned long long other = __shfl_xor_sync(0xFFFFFFFFu, best[e], o);
+      best[e] = other > best[e] ? other : best[e];
+    }
+  }
+  if (g == 0) {
+    kred[warp * 8 + 2 * t] = best[0];
+    kred[warp * 8 + 2 * t + 1] = best[1];
+  }
   __syncthreads();
   if (threadIdx.x < (unsigned)M) {
-    // column m is held by the lanes with t = m / 2, slot m % 2, of every warp
     const int m = threadIdx.x;
     unsigned long long b = 0ull;
-    for (int w = 0; w < kWarps; ++w)
-      for (int gg = 0; gg < 8; ++gg) {
-        const unsigned long long o = kred[(w * 32 + gg * 4 + m / 2) * 2 + (m & 1)];
-        b = o > b ? o : b;
-      }
+    for (int w = 0; w < kWarps; ++w) {
+      const unsigned long long o = kred[w * 8 + m];
+      b = o > b ? o : b;
+    }
     if (b != 0ull)
       asm volatile("red.relaxed.gpu.global.max.u64 [%0], %1;" ::"l"(p.keys + m), "l"(b) : "memory");
   }
@@ -591,6 +603,7 @@ struct Layout {
 };
 
 Layout layout_for(int warps, int m, int nchunks) {
+  const int kRing = ring_stages(m, warps);
   Layout l;
   size_t off = (size_t)nchunks * 8 * 4 * m * sizeof(uint2);  // B fragments
   l.off_red = (uint32_t)off;
@@ -599,7 +612,7 @@ Layout layout_for(int warps, int m, int nchunks) {
   off += (16 + 16 * warps + 8 + 16) * sizeof(float);
   off = (off + 15) & ~(size_t)15;
   l.off_kred = (uint32_t)off;
-  off += (size_t)warps * 32 * 2 * sizeof(unsigned long long);
+  off += (size_t)warps * 8 * sizeof(unsigned long long);
   off = (off + 1023) & ~(size_t)1023;
   l.off_ring = (uint32_t)off;
   off += (size_t)warps * kRing * kStageBytes;
