@@ -47,10 +47,9 @@ namespace {
 constexpr int kChunk = 128;       // K elements per chunk (64 packed bytes per row)
 constexpr int kItem = 2;          // chunks per stage (one TMA box of 16 rows x 128 bytes)
 constexpr int kStageBytes = 16 * 64 * kItem;
-// TMA stages per warp: batches of 4+ rows already hold one CTA per SM (their
-// staged activations are large), so they take a deeper ring; smaller batches
-// keep two CTAs per SM with two stages each.
-__host__ __device__ constexpr int ring_stages(int m, int warps) { return (warps >= 16 && m >= 4) ? 4 : 2; }
+// TMA stages per warp (two two-chunk boxes: 4 KB in flight per warp; deeper
+// rings measured no faster).
+__host__ __device__ constexpr int ring_stages(int, int) { return 2; }
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 constexpr int kL2Prefetch = 8;    // items per warp pulled into L2 while the previous call ends
 
