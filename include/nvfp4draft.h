@@ -64,6 +64,8 @@ extern "C" {
 #define W4A16_ARGMAX_WS_BYTES 128
 /* Workspace of nvfp4_quantize when its absmax output is NULL. */
 #define NVFP4_QUANTIZE_WS_BYTES 16
+/* Optional workspace of w4a16_gemm that enables its FP16 staging path. */
+#define W4A16_GEMM_WS_BYTES(m, k) ((size_t)(m) * (size_t)(k) * 2 + (size_t)(m) * 4 + 256)
 
 /* A quantised weight (all device pointers, 16-byte aligned). */
 typedef struct nvfp4_weight {
@@ -188,8 +190,17 @@ int w4a16_gemv_argmax_noalloc(const w4a16_act_segment *seg, int nseg, int m,
  *   m >= 1 (any; the last tile is masked); w->n % 128 == 0; w->k % 64 == 0.
  *   c_bf16   device BF16 [m, ldc], 16-byte aligned, ldc % 8 == 0, ldc >= n.
  *   w->scales 4-byte aligned.
- * Workspace: none.  Waits inside the kernel are bounded; one that runs out
- * writes NVFP4_ERR_TIMEOUT to ex->dev_status and leaves C incomplete.
+ * Workspace (optional): with at least W4A16_GEMM_WS_BYTES(m, k) bytes (16-byte
+ * aligned) the activations are first staged there as FP16, each row times an
+ * exact power of two that puts its largest magnitude in [2^14, 2^15) (exact
+ * for every activation within 2^-31 of the row maximum; smaller ones round at
+ * that level), and the weights are dequantised to FP16 with the hardware E2M1
+ * conversion for an FP16 x FP16 -> FP32 MMA; the row scale is removed from the
+ * FP32 sum.  Without it, the BF16 operands go to a BF16 MMA directly.  Both
+ * paths multiply exact weight values; they differ only in how activations far
+ * below their row's maximum are rounded.
+ * Waits inside the kernel are bounded; one that runs out writes
+ * NVFP4_ERR_TIMEOUT to ex->dev_status and leaves C incomplete.
  */
 int w4a16_gemm(const void *a_bf16, int64_t m, int64_t lda, const nvfp4_weight *w,
                void *c_bf16, int64_t ldc, const nvfp4_exec *ex);

@@ -230,13 +230,21 @@ def w4a16_gemv_argmax_noalloc(segments: Sequence, weight: Nvfp4Weight,
     return out_logits, out_argmax
 
 
+def gemm_workspace_bytes(m: int, k: int) -> int:
+    """Bytes of the optional w4a16_gemm workspace (FP16 staging path)."""
+    return m * k * 2 + m * 4 + 256
+
+
 def w4a16_gemm(a: torch.Tensor, weight: Nvfp4Weight, out: Optional[torch.Tensor] = None,
-               stream=None, dev_status: Optional[torch.Tensor] = None) -> torch.Tensor:
+               workspace: Optional[torch.Tensor] = None, stream=None,
+               dev_status: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Prefill GEMM.  Pass a workspace of gemm_workspace_bytes(m, k) bytes for
+    the FP16 staging path (see the header); without one the BF16 path runs."""
     assert a.dtype == torch.bfloat16 and a.dim() == 2 and a.stride(1) == 1 and a.is_cuda
     m = a.shape[0]
     if out is None:
         out = torch.empty((m, weight.n), dtype=torch.bfloat16, device=a.device)
-    ex = _exec(stream, None, dev_status)
+    ex = _exec(stream, workspace, dev_status)
     w = weight.c()
     rc = load().w4a16_gemm(a.data_ptr(), m, a.stride(0), ctypes.byref(w), out.data_ptr(),
                            out.stride(0), ctypes.byref(ex))

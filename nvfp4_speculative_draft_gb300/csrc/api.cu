@@ -194,7 +194,8 @@ int w4a16_gemm(const void* a_bf16, int64_t m, int64_t lda, const nvfp4_weight* w
   if (!aligned16(a_bf16) || !aligned16(c_bf16) || lda % 8 != 0 || ldc % 8 != 0 ||
       (reinterpret_cast<uintptr_t>(w->scales) & 3u))
     return NVFP4_ERR_ALIGN;
-  return launch_gemm(a_bf16, m, lda, w, c_bf16, ldc, status_of(ex), stream_of(ex));
+  return launch_gemm(a_bf16, m, lda, w, c_bf16, ldc, ex ? ex->workspace : nullptr,
+                     ex ? ex->workspace_bytes : 0, status_of(ex), stream_of(ex));
 }
 
 }  // extern "C"

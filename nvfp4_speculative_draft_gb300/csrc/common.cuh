@@ -66,4 +66,6 @@ int launch_gemv(const w4a16_act_segment* seg, int nseg, int m, const nvfp4_weigh
                 void* y, int y_dtype, int64_t ldy, bool want_argmax, int32_t* argmax,
                 void* workspace, int32_t* dev_status, cudaStream_t stream);
 int launch_gemm(const void* a, int64_t m, int64_t lda, const nvfp4_weight* w, void* c,
-                int64_t ldc, int32_t* dev_status, cudaStream_t stream);
+                int64_t ldc, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                cudaStream_t stream);
+size_t gemm_f16_workspace_bytes(int64_t m, int64_t k);

@@ -118,15 +118,17 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr) {
 // Instruction descriptor, kind::f16: D = F32 (bits 4..5 = 1), A = B = BF16
 // (bits 7..9 = 1, 10..12 = 1), both K-major, N >> 3 at bits 17..22, M >> 4 at
 // bits 24..28.
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
-                            ((uint32_t)(BM >> 4) << 24);
+constexpr uint32_t kIdescBf16 = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
+                                ((uint32_t)(BM >> 4) << 24);
+// The same with A = B = F16 (format 0 at bits 7..9 and 10..12).
+constexpr uint32_t kIdescF16 = (1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
 
-__device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
-                                         uint32_t accumulate) {
+__device__ __forceinline__ void mma_f16kind(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
       " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(tmem_d),
-      "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
@@ -196,6 +198,32 @@ __device__ __forceinline__ uint4 dequant_word(uint32_t q, uint32_t s) {
   return r;
 }
 
+__device__ __forceinline__ uint32_t f16x2_mul(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+// Two E4M3 scales (low byte first) -> F16 (exact), each replicated into both
+// halves of an f16x2.
+__device__ __forceinline__ void decode_scales_f16(uint32_t s2, uint32_t& lo, uint32_t& hi) {
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)s2, __NV_E4M3);
+  const uint32_t v = (uint32_t)h.x | ((uint32_t)h.y << 16);
+  lo = __byte_perm(v, 0, 0x1010);
+  hi = __byte_perm(v, 0, 0x3232);
+}
+// The 8 E2M1 codes of word q (natural order) -> 4 f16x2 by the hardware
+// conversion (byte j = elements 2j, 2j+1), times the block-scale pattern s:
+// every product is an exact F16 (at most 6 significant bits).
+__device__ __forceinline__ uint4 dequant_word_f16(uint32_t q, uint32_t s) {
+  uint32_t h0, h1, h2, h3;
+  asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n"
+      " cvt.rn.f16x2.e2m1x2 %0, b0;\n cvt.rn.f16x2.e2m1x2 %1, b1;\n"
+      " cvt.rn.f16x2.e2m1x2 %2, b2;\n cvt.rn.f16x2.e2m1x2 %3, b3;\n}"
+      : "=r"(h0), "=r"(h1), "=r"(h2), "=r"(h3)
+      : "r"(q));
+  return make_uint4(f16x2_mul(h0, s), f16x2_mul(h1, s), f16x2_mul(h2, s), f16x2_mul(h3, s));
+}
+
 struct GemmParams {
   const uint8_t* packed;
   const uint8_t* scales;
@@ -203,6 +231,7 @@ struct GemmParams {
   __nv_bfloat16* c;
   int64_t m, n, k, ldc;
   int mtiles, ntiles;
+  const float* row_inv;  // FP16 path: 2^-e of each activation row's staging scale
   int32_t* dev_status;
 };
 
@@ -213,8 +242,15 @@ __device__ __forceinline__ void tile_coords(const GemmParams& p, int t, int64_t&
   n0 = (int64_t)(t / p.mtiles) * BN;
 }
 
+// F16 = false: A is the caller's BF16 activations, B is dequantised to BF16.
+// F16 = true:  A is an FP16 copy of the activations, each row scaled by an
+//              exact power of two (staged by stage_a_f16 in the workspace), B is
+//              dequantised to FP16 with the hardware E2M1 conversion (fewer
+//              instructions per weight); the epilogue removes the row scale.
+template <bool F16>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ GemmParams p) {
+  constexpr uint32_t kIdesc = F16 ? kIdescF16 : kIdescBf16;
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;  // 128-byte swizzle wants 1 KB alignment
@@ -295,7 +331,7 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
           const uint64_t bd = smem_desc(base + s * kStageBytes + kABytes);
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk)  // advance 32 bytes (16 BF16) along K
-            mma_bf16(d, ad + 2 * kk, bd + 2 * kk, (kb > 0 || kk > 0) ? 1u : 0u);
+            mma_f16kind(d, ad + 2 * kk, bd + 2 * kk, kIdesc, (kb > 0 || kk > 0) ? 1u : 0u);
           mma_commit(empty(s));
         }
         mma_commit(tmem_full(ab));  // fires once the tile's MMAs have completed
@@ -352,12 +388,19 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
             ok = false;
           } else {
             uint32_t S0, S1;
-            decode_scales(cs, S0, S1);
+            if constexpr (F16)
+              decode_scales_f16(cs, S0, S1);
+            else
+              decode_scales(cs, S0, S1);
             const uint32_t words[4] = {c0.x, c0.y, c0.z, c0.w};
             unsigned char* brow = smem + s * kStageBytes + kABytes + r * 128;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {  // chunk 4h+j holds k = 32h + 8j .. +7
-              const uint4 v = dequant_word(words[j], j < 2 ? S0 : S1);
+              uint4 v;
+              if constexpr (F16)
+                v = dequant_word_f16(words[j], j < 2 ? S0 : S1);
+              else
+                v = dequant_word(words[j], j < 2 ? S0 : S1);
               *reinterpret_cast<uint4*>(brow + (((uint32_t)(4 * h + j) ^ swz) << 4)) = v;
             }
             fence_proxy_async();
@@ -371,7 +414,8 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
     // -------------------------------------------------------------- epilogue
     // warp quadrant q owns TMEM lanes 32q..32q+31 = rows 32q.. of the tile
     const int q = warp & 3;
-    const float gs = __ldg(p.gscale) * 256.0f;  // g * 2^8 (the dequant fold)
+    // BF16 path: g * 2^8 (the dequant fold); FP16 path: g, and 2^-e per row
+    const float gs = F16 ? __ldg(p.gscale) : __ldg(p.gscale) * 256.0f;
     for (int it = 0; it < my_tiles; ++it) {
       const int ab = it & 1;
       __syncwarp();
@@ -381,6 +425,7 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
       int64_t m0, n0;
       tile_coords(p, (int)blockIdx.x + it * (int)gridDim.x, m0, n0);
       const int64_t row = m0 + 32 * q + lane;
+      const float rs = (F16 && row < p.m) ? __ldg(p.row_inv + row) : 1.0f;
 #pragma unroll 1
       for (int j = 0; j < BN / 32; ++j) {
         const int col = 32 * j;
@@ -390,8 +435,8 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
           uint32_t packed16[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(v[2 * i]) * gs,
-                                                      __uint_as_float(v[2 * i + 1]) * gs);
+            __nv_bfloat162 b2 = __floats2bfloat162_rn((__uint_as_float(v[2 * i]) * rs) * gs,
+                                                      (__uint_as_float(v[2 * i + 1]) * rs) * gs);
             packed16[i] = *reinterpret_cast<uint32_t*>(&b2);
           }
           uint4* dst = reinterpret_cast<uint4*>(p.c + row * p.ldc + n0 + col);
@@ -416,17 +461,79 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
   }
 }
 
+// One CTA per activation row: FP16 copy of the row times 2^e, where e puts the
+// row's largest BF16 magnitude in [2^14, 2^15) (every activation within 2^-31
+// of it converts exactly: 8 significant bits, FP16 normal range); 2^-e kept for
+// the epilogue.  e is clamped to [-120, 120]; an all-zero row uses e = 0.
+constexpr int kStageThreads = 256;
+__global__ void __launch_bounds__(kStageThreads)
+stage_a_f16(const __nv_bfloat16* __restrict__ a, int64_t lda, int64_t k, __half* __restrict__ out,
+            float* __restrict__ row_inv) {
+  const int64_t row = blockIdx.x;
+  const uint4* src = reinterpret_cast<const uint4*>(a + row * lda);
+  uint4* dst = reinterpret_cast<uint4*>(out + row * k);
+  const int64_t nvec = k / 8;
+  uint32_t m2 = 0;
+  for (int64_t i = threadIdx.x; i < nvec; i += kStageThreads) {
+    const uint4 v = src[i];
+    m2 = __vmaxu2(m2, __vmaxu2(__vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu),
+                               __vmaxu2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu)));
+  }
+  uint32_t mx = max(m2 & 0xFFFFu, m2 >> 16);
+  mx = __reduce_max_sync(0xFFFFFFFFu, mx);
+  __shared__ uint32_t red[kStageThreads / 32];
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mx;
+  __syncthreads();
+  mx = 0;
+  for (int w = 0; w < kStageThreads / 32; ++w) mx = max(mx, red[w]);
+  const int ef = (int)(mx >> 7);
+  int e = mx == 0u ? 0 : 14 - (ef == 0 ? -126 : ef - 127);
+  e = e < -120 ? -120 : (e > 120 ? 120 : e);
+  const float sc = ldexpf(1.0f, e);
+  if (threadIdx.x == 0) row_inv[row] = ldexpf(1.0f, -e);
+  for (int64_t i = threadIdx.x; i < nvec; i += kStageThreads) {
+    const uint4 v = src[i];
+    const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const __half2 h = __floats2half2_rn(__uint_as_float(u[j] << 16) * sc,
+                                          __uint_as_float(u[j] & 0xFFFF0000u) * sc);
+      o[j] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    dst[i] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
 }  // namespace
 
+size_t gemm_f16_workspace_bytes(int64_t m, int64_t k) {
+  return (size_t)m * (size_t)k * 2 + (size_t)m * 4 + 256;
+}
+
 int launch_gemm(const void* a, int64_t m, int64_t lda, const nvfp4_weight* w, void* c,
-                int64_t ldc, int32_t* dev_status, cudaStream_t stream) {
+                int64_t ldc, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                cudaStream_t stream) {
+  // FP16 path when the workspace can hold the staged activations
+  const bool f16 = workspace != nullptr && workspace_bytes >= gemm_f16_workspace_bytes(m, w->k) &&
+                   nvfp4::aligned16(workspace) && m <= 0x7FFFFFFF;
+  __half* a16 = reinterpret_cast<__half*>(workspace);
+  float* row_inv = f16 ? reinterpret_cast<float*>(
+                             reinterpret_cast<char*>(workspace) + (((size_t)m * w->k * 2 + 15) & ~(size_t)15))
+                       : nullptr;
+  if (f16) {
+    stage_a_f16<<<(unsigned)m, kStageThreads, 0, stream>>>(
+        reinterpret_cast<const __nv_bfloat16*>(a), lda, w->k, a16, row_inv);
+    if (cudaGetLastError() != cudaSuccess) return NVFP4_ERR_CUDA;
+  }
   CUtensorMap tmap;
   const cuuint64_t dims[2] = {(cuuint64_t)w->k, (cuuint64_t)m};
-  const cuuint64_t strides[1] = {(cuuint64_t)lda * 2};
+  const cuuint64_t strides[1] = {(cuuint64_t)(f16 ? w->k : lda) * 2};
   const cuuint32_t box[2] = {BK, BM};
   const cuuint32_t estr[2] = {1, 1};
-  if (!nvfp4::encode_tiled(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(a), dims,
-                           strides, box, estr, CU_TENSOR_MAP_SWIZZLE_128B))
+  if (!nvfp4::encode_tiled(&tmap, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                           2, f16 ? static_cast<void*>(a16) : const_cast<void*>(a), dims, strides, box,
+                           estr, CU_TENSOR_MAP_SWIZZLE_128B))
     return NVFP4_ERR_CUDA;
   GemmParams p;
   p.packed = w->packed;
@@ -439,14 +546,16 @@ int launch_gemm(const void* a, int64_t m, int64_t lda, const nvfp4_weight* w, vo
   p.ldc = ldc;
   p.mtiles = (int)nvfp4::cdiv(m, BM);
   p.ntiles = (int)nvfp4::cdiv(w->n, BN);
+  p.row_inv = row_inv;
   p.dev_status = dev_status;
-  if (nvfp4::occupancy(reinterpret_cast<const void*>(gemm_tcgen05_kernel), kThreads, kSmemBytes) < 1)
+  auto kern = f16 ? gemm_tcgen05_kernel<true> : gemm_tcgen05_kernel<false>;
+  if (nvfp4::occupancy(reinterpret_cast<const void*>(kern), kThreads, kSmemBytes) < 1)
     return NVFP4_ERR_CUDA;
   const int64_t tiles = (int64_t)p.mtiles * p.ntiles;
   if (tiles > 0x7FFFFFFF) return NVFP4_ERR_SHAPE;
   const int sms = nvfp4::sm_count();
   const unsigned grid = (unsigned)(tiles < sms ? tiles : sms);  // persistent: one CTA per SM
-  gemm_tcgen05_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tmap, p);
+  kern<<<grid, kThreads, kSmemBytes, stream>>>(tmap, p);
   if (cudaGetLastError() != cudaSuccess) return NVFP4_ERR_CUDA;
   return NVFP4_OK;
 }

@@ -5,7 +5,8 @@
 Cases (seeded synthetic inputs of the draft head's workloads, built on the
 device): ``lm_head`` (32768 x 4096, RMSNorm + GEMV + argmax, M=1), ``propose``
 (151936 x 5120 GEMV + argmax, M=--m), ``fc`` (5120 x 10240, two RMSNorms +
-concat, BF16 out, M=--m), ``gemm`` (2048 x 17408 x 5120 prefill GEMM),
+concat, BF16 out, M=--m), ``gemm`` (2048 x 17408 x 5120 prefill GEMM, FP16
+staging workspace as the benchmark times it),
 ``quantize`` (17408 x 5120).  Inputs are prepared first (their kernels run
 before the measured calls, so ``ncu -k regex:<kernel> -s <n>`` can skip them),
 then the call runs --iters times and the process exits 0.
@@ -59,9 +60,10 @@ def main():
     elif args.case == "gemm":
         c = workloads.prefill_gemm(device=dev)
         wq, _ = nd.nvfp4_quantize(c.w)
+        ws = torch.empty(nd.gemm_workspace_bytes(2048, 5120), dtype=torch.uint8, device=dev)
         torch.cuda.synchronize()
         for _ in range(args.iters):
-            nd.w4a16_gemm(c.a, wq)
+            nd.w4a16_gemm(c.a, wq, workspace=ws)
     else:
         c = workloads.prefill_gemm(m=128, device=dev)
         torch.cuda.synchronize()

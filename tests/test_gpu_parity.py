@@ -265,14 +265,17 @@ def check_gemm(a, wq_oracle, c_gpu, rows, cols):
                           f"gpu {got[bad[0]]} oracle {exact[bad[0]]}"
 
 
+@pytest.mark.parametrize("staged", [False, True], ids=["bf16", "f16_staged"])
 @pytest.mark.parametrize("m_rows,n,k", [(128, 128, 64), (200, 256, 320), (1, 384, 128),
                                         (257, 128, 1024)])
-def test_gemm_small_all_outputs(dev, m_rows, n, k):
+def test_gemm_small_all_outputs(dev, m_rows, n, k, staged):
     m = nd()
     case = workloads.prefill_gemm(m=m_rows, n=n, k=k)
     p, s, g, _ = oracle.quantize(workloads.bits(case.w))
     wq = upload_weight(p, s, g, dev)
-    c = m.w4a16_gemm(case.a.to(dev), wq)
+    ws = (torch.empty(m.gemm_workspace_bytes(m_rows, k), dtype=torch.uint8, device=dev)
+          if staged else None)
+    c = m.w4a16_gemm(case.a.to(dev), wq, workspace=ws)
     torch.cuda.synchronize()
     cg = c.float().cpu().numpy()
     rows = np.repeat(np.arange(m_rows), n)
@@ -293,3 +296,24 @@ def test_gemm_strided_output(dev):
     rows = np.repeat(np.arange(130), 256)
     cols = np.tile(np.arange(256), 130)
     check_gemm(case.a, (p, s, g), o, rows, cols)
+
+
+def test_gemm_staged_rows_of_very_different_scales(dev):
+    """Rows whose magnitudes differ by up to 2^60: each row gets its own FP16
+    staging scale, so both paths stay within tolerance of the oracle."""
+    m = nd()
+    case = workloads.prefill_gemm(m=130, n=256, k=192)
+    a = case.a.float()
+    a *= torch.exp2(torch.linspace(-30, 30, 130)).unsqueeze(1)
+    a = a.to(torch.bfloat16)
+    a[7] = 0
+    p, s, g, _ = oracle.quantize(workloads.bits(case.w))
+    wq = upload_weight(p, s, g, dev)
+    rows = np.repeat(np.arange(130), 256)
+    cols = np.tile(np.arange(256), 130)
+    for staged in (False, True):
+        ws = (torch.empty(m.gemm_workspace_bytes(130, 192), dtype=torch.uint8, device=dev)
+              if staged else None)
+        c = m.w4a16_gemm(a.to(dev), wq, workspace=ws)
+        torch.cuda.synchronize()
+        check_gemm(a, (p, s, g), c.float().cpu().numpy(), rows, cols)
