@@ -10,7 +10,7 @@
 // One CTA computes a 128 x 256 output tile (M = 128 activation rows, N = 256
 // weight rows) with tcgen05.mma (cta_group::1, kind::f16, BF16 x BF16 -> FP32),
 // the accumulator in tensor memory (256 TMEM columns).  K runs in steps of 64
-// through a 4-stage shared-memory ring:
+// through shared-memory rings (7 stages of A, 3 of B):
 //   warp 0      TMA producer: the 128 x 64 BF16 A tile by cp.async.bulk.tensor
 //               (128-byte swizzle; rows past m read as zero);
 //   warp 1      allocates TMEM, issues the 4 MMAs (K = 16 each) of a stage from
@@ -36,16 +36,18 @@
 namespace {
 
 constexpr int BM = 128, BN = 256, BK = 64;
-constexpr int kStages = 4;
+constexpr int kStagesA = 7;  // A tiles arrive by TMA from L2: a deep ring hides its latency
+constexpr int kStagesB = 3;  // B tiles are written by the dequantising warps
 constexpr int kABytes = BM * BK * 2;  // 16 KB
 constexpr int kBBytes = BN * BK * 2;  // 32 KB
-constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kRingABytes = kStagesA * kABytes;
+constexpr int kRingBytes = kRingABytes + kStagesB * kBBytes;
 constexpr int kDequantWarps = 16;  // two threads per weight row, 32 K-elements each
 constexpr int kEpilogueWarps = 4;
 constexpr int kThreads = (2 + kDequantWarps + kEpilogueWarps) * 32;
 constexpr int kTmemCols = 2 * BN;  // two accumulators: epilogue of one tile overlaps the next
 constexpr int kPrefetch = 4;       // k steps of weight rows in flight per dequant thread
-constexpr size_t kSmemBytes = 1024 /*alignment slack*/ + (size_t)kStages * kStageBytes + 256;
+constexpr size_t kSmemBytes = 1024 /*alignment slack*/ + (size_t)kRingBytes + 256;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
 // ------------------------------------------------------------ PTX helpers
@@ -255,14 +257,18 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;  // 128-byte swizzle wants 1 KB alignment
   unsigned char* const smem = smem_raw + (base - raw);
-  const uint32_t bars = base + kStages * kStageBytes;
+  // ring layout: kStagesA A tiles, then kStagesB B tiles (all 1 KB aligned)
+  auto a_tile = [&](int s) { return base + (uint32_t)(s * kABytes); };
+  auto b_tile = [&](int s) { return (uint32_t)(kRingABytes + s * kBBytes); };  // offset from base
+  const uint32_t bars = base + kRingBytes;
   auto full_a = [&](int s) { return bars + 8u * s; };
-  auto full_b = [&](int s) { return bars + 8u * (kStages + s); };
-  auto empty = [&](int s) { return bars + 8u * (2 * kStages + s); };
-  auto tmem_full = [&](int b) { return bars + 8u * (3 * kStages + b); };
-  auto tmem_empty = [&](int b) { return bars + 8u * (3 * kStages + 2 + b); };
-  uint32_t* tmem_slot =
-      reinterpret_cast<uint32_t*>(smem + kStages * kStageBytes + 8 * (3 * kStages + 4));
+  auto empty_a = [&](int s) { return bars + 8u * (kStagesA + s); };
+  auto full_b = [&](int s) { return bars + 8u * (2 * kStagesA + s); };
+  auto empty_b = [&](int s) { return bars + 8u * (2 * kStagesA + kStagesB + s); };
+  constexpr int kNbar = 2 * kStagesA + 2 * kStagesB;
+  auto tmem_full = [&](int b) { return bars + 8u * (kNbar + b); };
+  auto tmem_empty = [&](int b) { return bars + 8u * (kNbar + 2 + b); };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kRingBytes + 8 * (kNbar + 4));
   volatile uint32_t* abort = tmem_slot + 1;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -274,10 +280,13 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
   const int total = my_tiles * nk;  // k steps streamed through the ring
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kStagesA; ++s) {
       mbar_init(full_a(s), 1);
+      mbar_init(empty_a(s), 1);
+    }
+    for (int s = 0; s < kStagesB; ++s) {
       mbar_init(full_b(s), kDequantWarps);
-      mbar_init(empty(s), 1);
+      mbar_init(empty_b(s), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tmem_full(b), 1);
@@ -302,13 +311,13 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
     // ---------------------------------------------------------- TMA producer
     if (lane == 0) {
       for (int g = 0; g < total; ++g) {
-        const int s = g % kStages, r = g / kStages;
+        const int s = g % kStagesA, r = g / kStagesA;
         const int kb = g % nk;
         int64_t m0, n0;
         tile_coords(p, (int)blockIdx.x + (g / nk) * (int)gridDim.x, m0, n0);
-        if (r > 0 && !mbar_wait(empty(s), (r - 1) & 1, abort, p.dev_status)) break;
+        if (r > 0 && !mbar_wait(empty_a(s), (r - 1) & 1, abort, p.dev_status)) break;
         mbar_arrive_expect_tx(full_a(s), kABytes);
-        tma_load_2d(base + s * kStageBytes, &tmap_a, kb * BK, (int)m0, full_a(s));
+        tma_load_2d(a_tile(s), &tmap_a, kb * BK, (int)m0, full_a(s));
       }
     }
   } else if (warp == 1) {
@@ -322,17 +331,19 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
         const uint32_t d = tmem + (uint32_t)(ab * BN);
         for (int kb = 0; kb < nk; ++kb) {
           const int g = it * nk + kb;
-          const int s = g % kStages, r = g / kStages;
-          ok = mbar_wait(full_a(s), r & 1, abort, p.dev_status) &&
-               mbar_wait(full_b(s), r & 1, abort, p.dev_status);
+          const int sa = g % kStagesA, ra = g / kStagesA;
+          const int sb = g % kStagesB, rb = g / kStagesB;
+          ok = mbar_wait(full_a(sa), ra & 1, abort, p.dev_status) &&
+               mbar_wait(full_b(sb), rb & 1, abort, p.dev_status);
           if (!ok) break;
           tc_fence_after();
-          const uint64_t ad = smem_desc(base + s * kStageBytes);
-          const uint64_t bd = smem_desc(base + s * kStageBytes + kABytes);
+          const uint64_t ad = smem_desc(a_tile(sa));
+          const uint64_t bd = smem_desc(base + b_tile(sb));
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk)  // advance 32 bytes (16 BF16) along K
             mma_f16kind(d, ad + 2 * kk, bd + 2 * kk, kIdesc, (kb > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(empty(s));
+          mma_commit(empty_a(sa));  // both commits track the same MMAs
+          mma_commit(empty_b(sb));
         }
         mma_commit(tmem_full(ab));  // fires once the tile's MMAs have completed
       }
@@ -380,11 +391,11 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
       for (int i = 0; i < kPrefetch; ++i) {
         const int g = g0 + i;
         if (g < total && ok) {
-          const int s = g % kStages, rr = g / kStages;
+          const int s = g % kStagesB, rr = g / kStagesB;
           const uint4 c0 = qa[i];
           const uint32_t cs = qs[i];
           if (g + kPrefetch < total) issue(i);
-          if (rr > 0 && !mbar_wait(empty(s), (rr - 1) & 1, abort, p.dev_status)) {
+          if (rr > 0 && !mbar_wait(empty_b(s), (rr - 1) & 1, abort, p.dev_status)) {
             ok = false;
           } else {
             uint32_t S0, S1;
@@ -393,7 +404,7 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
             else
               decode_scales(cs, S0, S1);
             const uint32_t words[4] = {c0.x, c0.y, c0.z, c0.w};
-            unsigned char* brow = smem + s * kStageBytes + kABytes + r * 128;
+            unsigned char* brow = smem + b_tile(s) + r * 128;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {  // chunk 4h+j holds k = 32h + 8j .. +7
               uint4 v;
