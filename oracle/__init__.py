@@ -74,6 +74,11 @@ def lib():
         L.oracle_gemm_pairs.argtypes = [_u16p, _i64, _u8p, _u8p, ctypes.c_float, _i64,
                                         _i64p, _i64p, _i64, _f64p, _f64p]
         L.oracle_gemm_pairs.restype = None
+        _i32p = ctypes.POINTER(ctypes.c_int32)
+        L.oracle_argmax_masked.argtypes = [_f64p, _i64, _i32p, _i64]
+        L.oracle_argmax_masked.restype = _i64
+        L.oracle_top1_logprob.argtypes = [_f64p, _i64, _i32p, _i64, _i64]
+        L.oracle_top1_logprob.restype = ctypes.c_double
         _LIB = L
     return _LIB
 
@@ -246,3 +251,24 @@ def gemm_pairs(a_bits, packed, scales, g, rows, cols):
                             float(g), k, _ptr(rows, _i64p), _ptr(cols, _i64p), rows.size,
                             _ptr(exact, _f64p), _ptr(sabs, _f64p))
     return exact, sabs
+
+
+def argmax_masked(y, mask=None) -> int:
+    """Grammar-masked argmax (mask: int32 words, bit i%32 of word i/32)."""
+    y = _c(y, np.float64)
+    if mask is None:
+        return int(lib().oracle_argmax_masked(_ptr(y, _f64p), y.size, None, 0))
+    mask = _c(mask, np.int32)
+    return int(lib().oracle_argmax_masked(_ptr(y, _f64p), y.size,
+                                          _ptr(mask, ctypes.POINTER(ctypes.c_int32)), mask.size))
+
+
+def top1_logprob(y, idx, mask=None) -> float:
+    """y[idx] - logsumexp over the allowed tokens; NaN when none is allowed."""
+    y = _c(y, np.float64)
+    if mask is None:
+        return float(lib().oracle_top1_logprob(_ptr(y, _f64p), y.size, None, 0, int(idx)))
+    mask = _c(mask, np.int32)
+    return float(lib().oracle_top1_logprob(_ptr(y, _f64p), y.size,
+                                           _ptr(mask, ctypes.POINTER(ctypes.c_int32)), mask.size,
+                                           int(idx)))

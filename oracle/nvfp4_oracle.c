@@ -356,3 +356,62 @@ void oracle_gemm_pairs(const uint16_t *A, int64_t lda, const uint8_t *packed,
         sabs[p] = aacc;
     }
 }
+
+/* ------------------------------------------------- masked argmax, log-prob */
+
+/* Grammar-masked greedy argmax ("spark_model/layers/deepseek_v4_mtp.rs",
+ * argmax_grammar_masked): token i takes part only when bit i%32 of word i/32
+ * of the mask is set (words past nwords disallow); among those, the strict '>'
+ * ascending scan from -inf.  Returns 0 when no token is allowed.  mask may be
+ * NULL (every token allowed). */
+int64_t oracle_argmax_masked(const double *y, int64_t n, const int32_t *mask, int64_t nwords)
+{
+    int64_t best = 0;
+    double bestv = -INFINITY;
+    int any = 0;
+    for (int64_t i = 0; i < n; ++i) {
+        if (mask != NULL) {
+            int64_t word = i / 32;
+            if (word >= nwords || ((mask[word] >> (i % 32)) & 1) == 0)
+                continue;
+        }
+        any = 1;
+        if (y[i] > bestv) {
+            bestv = y[i];
+            best = i;
+        }
+    }
+    return any ? best : 0;
+}
+
+/* Top-1 log-probability of token idx under softmax over the allowed tokens:
+ * y[idx] - log(sum_j exp(y[j])), the sum taken in binary64 after subtracting
+ * the largest allowed logit.  NaN when no token is allowed. */
+double oracle_top1_logprob(const double *y, int64_t n, const int32_t *mask, int64_t nwords,
+                           int64_t idx)
+{
+    double mx = -INFINITY;
+    int any = 0;
+    for (int64_t i = 0; i < n; ++i) {
+        if (mask != NULL) {
+            int64_t word = i / 32;
+            if (word >= nwords || ((mask[word] >> (i % 32)) & 1) == 0)
+                continue;
+        }
+        any = 1;
+        if (y[i] > mx)
+            mx = y[i];
+    }
+    if (!any)
+        return NAN;
+    double s = 0.0;
+    for (int64_t i = 0; i < n; ++i) {
+        if (mask != NULL) {
+            int64_t word = i / 32;
+            if (word >= nwords || ((mask[word] >> (i % 32)) & 1) == 0)
+                continue;
+        }
+        s += exp(y[i] - mx);
+    }
+    return y[idx] - (mx + log(s));
+}

@@ -348,3 +348,51 @@ def test_workloads_are_seeded_and_shaped():
     assert a.extra["outlier_rows"].numel() == 3
     c = workloads.fc_combiner(n=32, k_seg=48, m=3)
     assert c.w.shape == (32, 96) and len(c.segments) == 2
+
+
+# ------------------------------------------- masked argmax and top-1 log-prob
+
+def _bits_to_mask(allowed):
+    n = len(allowed)
+    words = np.zeros((n + 31) // 32, dtype=np.int64)
+    for i, a in enumerate(allowed):
+        if a:
+            words[i // 32] |= 1 << (i % 32)
+    return words.astype(np.uint32).view(np.int32)
+
+
+def test_masked_argmax_brute_force_and_scan_rules():
+    rng = np.random.default_rng(21)
+    for _ in range(50):
+        n = int(rng.integers(1, 200))
+        y = rng.integers(-4, 4, size=n).astype(np.float64)
+        allowed = rng.random(n) < 0.3
+        mask = _bits_to_mask(allowed)
+        idxs = np.nonzero(allowed)[0]
+        exp = int(idxs[np.argmax(y[idxs])]) if idxs.size else 0   # first max among allowed
+        assert oracle.argmax_masked(y, mask) == exp
+    assert oracle.argmax_masked(np.array([5.0, 1.0]), _bits_to_mask([False, False])) == 0
+    # words past the mask's length disallow their tokens
+    y = np.zeros(40); y[35] = 9.0
+    assert oracle.argmax_masked(y, _bits_to_mask([True] * 32)) == 0
+    assert oracle.argmax_masked(np.array([np.nan, 2.0, 7.0]), _bits_to_mask([True, True, False])) == 1
+
+
+def test_top1_logprob_against_scipy_logsumexp():
+    from scipy.special import logsumexp
+    rng = np.random.default_rng(22)
+    for _ in range(30):
+        n = int(rng.integers(1, 3000))
+        y = rng.standard_normal(n) * 8
+        i = int(np.argmax(y))
+        assert abs(oracle.top1_logprob(y, i) - (y[i] - logsumexp(y))) < 1e-12 * (1 + abs(y[i]))
+        allowed = rng.random(n) < 0.5
+        allowed[i] = True
+        mask = _bits_to_mask(allowed)
+        exp = y[i] - logsumexp(y[allowed])
+        assert abs(oracle.top1_logprob(y, i, mask) - exp) < 1e-12 * (1 + abs(y[i]))
+    assert np.isnan(oracle.top1_logprob(np.array([1.0, 2.0]), 0, _bits_to_mask([False, False])))
+    # a single allowed token has probability one
+    assert oracle.top1_logprob(np.array([3.0, 50.0]), 0, _bits_to_mask([True, False])) == 0.0
+    # uniform logits: log(1/n)
+    assert abs(oracle.top1_logprob(np.zeros(64), 5) - np.log(1 / 64)) < 1e-15
