@@ -62,6 +62,10 @@ extern "C" {
 /* Workspace of w4a16_gemv_argmax: W4A16_GEMV_MAX_M 64-bit keys + a counter.
  * Zero it once when allocated; every completed call leaves it zeroed. */
 #define W4A16_ARGMAX_WS_BYTES 128
+/* Most CTAs a GEMV launch uses, and the workspace of w4a16_gemv_argmax_ex
+ * (keys + counter, then one (max, sum) pair per CTA and batch row). */
+#define W4A16_GEMV_MAX_CTAS 1024
+#define W4A16_ARGMAX_EX_WS_BYTES (128 + W4A16_GEMV_MAX_CTAS * 8 * 8)
 /* Workspace of nvfp4_quantize when its absmax output is NULL. */
 #define NVFP4_QUANTIZE_WS_BYTES 16
 /* Optional workspace of w4a16_gemm that enables its FP16 staging path. */
@@ -155,6 +159,30 @@ int w4a16_gemv(const w4a16_act_segment *seg, int nseg, int m, const nvfp4_weight
 int w4a16_gemv_argmax(const w4a16_act_segment *seg, int nseg, int m,
                       const nvfp4_weight *w, float *logits, int64_t ld_logits,
                       int32_t *argmax, const nvfp4_exec *ex);
+
+/*
+ * w4a16_gemv_argmax_ex -- w4a16_gemv_argmax with the two outputs the draft
+ * loop asks of the LM head besides the token id:
+ *   mask      device int32 [m, ld_mask] or NULL: grammar bitmask, bit n%32 of
+ *             word n/32 of row r allows token n for batch row r (ld_mask >=
+ *             ceil(n/32)).  A disallowed token never wins; a row with no
+ *             allowed token returns index 0 -- the masked scan of
+ *             argmax_grammar_masked in "spark_model/layers/deepseek_v4_mtp.rs",
+ *             fused into the GEMV instead of run on the host.  Logits are
+ *             written unmasked.
+ *   logprob   device float [m] or NULL: top-1 log-probability of the chosen
+ *             token, y[argmax] - log(sum exp(y)) over the allowed tokens; NaN
+ *             when no token is allowed.  It is what the batched
+ *             argmax_bf16_batch_lp kernel of "metrale_model_layers/layers/
+ *             mtp_head.rs" (MtpHead fields) writes per row, and what the draft
+ *             confidence stop there reads (last_conf_bits).  FP32 exp/log; the
+ *             per-CTA partials are combined in a fixed order.
+ * Workspace: W4A16_ARGMAX_EX_WS_BYTES, 16-byte aligned, zeroed once when
+ * allocated (each completed call re-zeroes its first 128 bytes).
+ */
+int w4a16_gemv_argmax_ex(const w4a16_act_segment *seg, int nseg, int m, const nvfp4_weight *w,
+                         float *logits, int64_t ld_logits, int32_t *argmax, float *logprob,
+                         const int32_t *mask, int64_t ld_mask, const nvfp4_exec *ex);
 
 /*
  * w4a16_gemv_argmax_noalloc -- w4a16_gemv_argmax for callers that cannot

@@ -11,6 +11,7 @@ The four calls keep the C names:
 * :func:`nvfp4_quantize`     BF16 [n, k] -> NVFP4 (packed, scales, g, absmax)
 * :func:`w4a16_gemv`         y[m, n] = g * a . w~   (m <= 8, RMSNorm/concat fused)
 * :func:`w4a16_gemv_argmax`  the same, FP32 logits + fused greedy argmax
+* :func:`w4a16_gemv_argmax_ex`  + grammar bitmask and top-1 log-probability
 * :func:`w4a16_gemm`         prefill C[m, n] = bf16(g * A . w~^T)
 """
 import ctypes
@@ -31,8 +32,11 @@ DTYPE_BF16 = 1
 GEMV_MAX_M = 8
 GEMV_MAX_K = 16384
 ARGMAX_WS_BYTES = 128
+GEMV_MAX_CTAS = 1024
+ARGMAX_EX_WS_BYTES = 128 + GEMV_MAX_CTAS * 8 * 8
 QUANTIZE_WS_BYTES = 16
-EXPORTED = ("nvfp4_quantize", "w4a16_gemv", "w4a16_gemv_argmax", "w4a16_gemm")
+EXPORTED = ("nvfp4_quantize", "w4a16_gemv", "w4a16_gemv_argmax", "w4a16_gemv_argmax_ex",
+            "w4a16_gemm")
 
 
 class Nvfp4Error(RuntimeError):
@@ -74,6 +78,8 @@ def load(path: str = LIB_PATH):
     L.nvfp4_quantize.argtypes = [vp, i64, i64, vp, vp, vp, vp, P(_Exec)]
     L.w4a16_gemv.argtypes = [P(_Segment), i32, i32, P(_Weight), vp, i32, i64, P(_Exec)]
     L.w4a16_gemv_argmax.argtypes = [P(_Segment), i32, i32, P(_Weight), vp, i64, vp, P(_Exec)]
+    L.w4a16_gemv_argmax_ex.argtypes = [P(_Segment), i32, i32, P(_Weight), vp, i64, vp, vp, vp,
+                                       i64, P(_Exec)]
     L.w4a16_gemm.argtypes = [vp, i64, i64, P(_Weight), vp, i64, P(_Exec)]
     L.w4a16_gemv_argmax_noalloc.argtypes = [P(_Segment), i32, i32, P(_Weight), vp, i64, vp, vp,
                                             vp]
@@ -115,12 +121,13 @@ _WS = {}
 
 
 def argmax_workspace(device) -> torch.Tensor:
-    """A zeroed argmax workspace per device (each completed call re-zeroes it).
-    Calls on concurrent streams must pass their own workspace instead."""
+    """A zeroed argmax workspace per device (each completed call re-zeroes it),
+    large enough for :func:`w4a16_gemv_argmax_ex`.  Calls on concurrent
+    streams must pass their own workspace instead."""
     device = torch.device(device)
     key = ("argmax", device.index)
     if key not in _WS:
-        _WS[key] = torch.zeros(ARGMAX_WS_BYTES, dtype=torch.uint8, device=device)
+        _WS[key] = torch.zeros(ARGMAX_EX_WS_BYTES, dtype=torch.uint8, device=device)
     return _WS[key]
 
 
@@ -204,6 +211,51 @@ def w4a16_gemv_argmax(segments: Sequence, weight: Nvfp4Weight, logits: bool = Tr
                                   out_argmax.data_ptr(), ctypes.byref(ex))
     _check("w4a16_gemv_argmax", rc)
     return out_logits, out_argmax
+
+
+def pack_mask(allowed: torch.Tensor) -> torch.Tensor:
+    """Bool [m, n] -> int32 words [m, ceil(n/32)], bit j%32 of word j/32 = allowed[:, j]."""
+    m, n = allowed.shape
+    nw = (n + 31) // 32
+    bits = torch.zeros((m, nw * 32), dtype=torch.int64, device=allowed.device)
+    bits[:, :n] = allowed.to(torch.int64)
+    words = (bits.view(m, nw, 32) << torch.arange(32, device=allowed.device)).sum(-1)
+    return torch.where(words >= 2 ** 31, words - 2 ** 32, words).to(torch.int32)
+
+
+def w4a16_gemv_argmax_ex(segments: Sequence, weight: Nvfp4Weight, mask: Optional[torch.Tensor] = None,
+                         logprob: bool = True, logits: bool = True,
+                         out_logits: Optional[torch.Tensor] = None,
+                         out_argmax: Optional[torch.Tensor] = None,
+                         out_logprob: Optional[torch.Tensor] = None,
+                         workspace: Optional[torch.Tensor] = None, stream=None,
+                         dev_status: Optional[torch.Tensor] = None):
+    """Returns (logits FP32 [m, n] or None, argmax int32 [m], logprob FP32 [m] or None).
+
+    ``mask`` is int32 words [m, >= ceil(n/32)] (see :func:`pack_mask`) or None."""
+    segs, m = _segments(segments)
+    dev = weight.packed.device
+    if logits and out_logits is None:
+        out_logits = torch.empty((m, weight.n), dtype=torch.float32, device=dev)
+    if out_argmax is None:
+        out_argmax = torch.empty(m, dtype=torch.int32, device=dev)
+    if logprob and out_logprob is None:
+        out_logprob = torch.empty(m, dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = argmax_workspace(dev)
+    if mask is not None and (mask.dtype != torch.int32 or mask.stride(1) != 1 or mask.shape[0] < m):
+        raise ValueError("mask must be int32 [m, words] with unit column stride")
+    ex = _exec(stream, workspace, dev_status)
+    w = weight.c()
+    rc = load().w4a16_gemv_argmax_ex(segs, len(segments), m, ctypes.byref(w),
+                                     out_logits.data_ptr() if out_logits is not None else None,
+                                     out_logits.stride(0) if out_logits is not None else 0,
+                                     out_argmax.data_ptr(),
+                                     out_logprob.data_ptr() if out_logprob is not None else None,
+                                     mask.data_ptr() if mask is not None else None,
+                                     mask.stride(0) if mask is not None else 0, ctypes.byref(ex))
+    _check("w4a16_gemv_argmax_ex", rc)
+    return out_logits, out_argmax, out_logprob
 
 
 def w4a16_gemv_argmax_noalloc(segments: Sequence, weight: Nvfp4Weight,

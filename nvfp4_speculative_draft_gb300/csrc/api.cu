@@ -184,6 +184,29 @@ int w4a16_gemv_argmax(const w4a16_act_segment* seg, int nseg, int m, const nvfp4
                      ex->workspace, status_of(ex), stream_of(ex));
 }
 
+int w4a16_gemv_argmax_ex(const w4a16_act_segment* seg, int nseg, int m, const nvfp4_weight* w,
+                         float* logits, int64_t ld_logits, int32_t* argmax, float* logprob,
+                         const int32_t* mask, int64_t ld_mask, const nvfp4_exec* ex) {
+  int rc = check_weight(w);
+  if (rc) return rc;
+  rc = check_segments(seg, nseg, m, w->k);
+  if (rc) return rc;
+  if (argmax == nullptr) return NVFP4_ERR_NULL;
+  if ((reinterpret_cast<uintptr_t>(argmax) & 3u) ||
+      (logits != nullptr && (reinterpret_cast<uintptr_t>(logits) & 3u)) ||
+      (logprob != nullptr && (reinterpret_cast<uintptr_t>(logprob) & 3u)) ||
+      (mask != nullptr && (reinterpret_cast<uintptr_t>(mask) & 3u)))
+    return NVFP4_ERR_ALIGN;
+  if (logits != nullptr && ld_logits < w->n) return NVFP4_ERR_SHAPE;
+  if (mask != nullptr && ld_mask < (w->n + 31) / 32) return NVFP4_ERR_SHAPE;
+  if (w->n > 0x7FFFFFFFLL) return NVFP4_ERR_SHAPE;
+  if (ex == nullptr || ex->workspace == nullptr || ex->workspace_bytes < W4A16_ARGMAX_EX_WS_BYTES ||
+      !aligned16(ex->workspace))
+    return NVFP4_ERR_WORKSPACE;
+  return launch_gemv(seg, nseg, m, w, logits, NVFP4_DTYPE_F32, ld_logits, true, argmax,
+                     ex->workspace, status_of(ex), stream_of(ex), logprob, mask, ld_mask);
+}
+
 int w4a16_gemm(const void* a_bf16, int64_t m, int64_t lda, const nvfp4_weight* w, void* c_bf16,
                int64_t ldc, const nvfp4_exec* ex) {
   int rc = check_weight(w);

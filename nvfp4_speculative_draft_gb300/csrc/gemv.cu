@@ -70,6 +70,10 @@ struct GemvParams {
   unsigned long long* keys;  // argmax mode when non-null
   unsigned int* counter;
   int32_t* argmax;
+  float* logprob;            // top-1 log-probability per batch row, or null
+  float2* lse;               // per-CTA (max, sum) log-sum-exp partials [grid][8]
+  const int32_t* mask;       // grammar bitmask [m][ld_mask] int32 words, or null
+  int64_t ld_mask;
   int32_t* dev_status;
   int ks;          // warps sharing one 16-row tile (split K)
   int64_t ntiles;  // ceil(n / 16)
@@ -193,6 +197,14 @@ __device__ __forceinline__ unsigned long long argmax_key(float v, uint32_t idx) 
   uint32_t b = (v == 0.0f) ? 0u : __float_as_uint(v);
   uint32_t o = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
   return ((unsigned long long)o << 32) | (unsigned long long)(0xFFFFFFFFu - idx);
+}
+
+// (m, s) <- log-sum-exp merge of (m, s) and (om, os), s the sum of exp(x - m).
+__device__ __forceinline__ void lse_merge(float& m, float& s, float om, float os) {
+  const float nm = fmaxf(m, om);
+  if (nm == -INFINITY) return;  // both empty
+  s = s * expf(m - nm) + os * expf(om - nm);
+  m = nm;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -449,6 +461,7 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
   const float inv1 = row_scale_pow2(rowmax[min(2 * t + 1, M - 1)], true);
   const uint2* bbase = bfrag + (lane % BSTRIDE);
   unsigned long long best[2] = {0ull, 0ull};  // running argmax keys, columns 2t and 2t+1
+  float lm[2] = {-INFINITY, -INFINITY}, ls[2] = {0.f, 0.f};  // log-sum-exp (max, sum)
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
   int ct = 0, cc = 0;  // compute cursor
 
@@ -490,8 +503,21 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
               reinterpret_cast<__nv_bfloat16*>(p.y)[mm * p.ldy + rows[h]] = __float2bfloat16_rn(v);
           }
           if (p.keys != nullptr) {
-            const unsigned long long key = argmax_key(v, (uint32_t)rows[h]);
-            best[e] = key > best[e] ? key : best[e];
+            const bool allowed =
+                p.mask == nullptr ||
+                ((__ldg(p.mask + mm * p.ld_mask + (rows[h] >> 5)) >> (rows[h] & 31)) & 1);
+            if (allowed) {
+              const unsigned long long key = argmax_key(v, (uint32_t)rows[h]);
+              best[e] = key > best[e] ? key : best[e];
+              if (p.logprob != nullptr) {  // online log-sum-exp over the allowed logits
+                if (v > lm[e]) {
+                  ls[e] = ls[e] * expf(lm[e] - v) + 1.0f;
+                  lm[e] = v;
+                } else {
+                  ls[e] += expf(v - lm[e]);
+                }
+              }
+            }
           }
         }
       }
@@ -541,9 +567,25 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
       best[e] = other > best[e] ? other : best[e];
     }
   }
+  float2* lred = reinterpret_cast<float2*>(kred + kWarps * 8);  // [kWarps][8]
+  if (p.logprob != nullptr) {
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        const float om = __shfl_xor_sync(0xFFFFFFFFu, lm[e], o);
+        const float os = __shfl_xor_sync(0xFFFFFFFFu, ls[e], o);
+        lse_merge(lm[e], ls[e], om, os);
+      }
+    }
+  }
   if (g == 0) {
     kred[warp * 8 + 2 * t] = best[0];
     kred[warp * 8 + 2 * t + 1] = best[1];
+    if (p.logprob != nullptr) {
+      lred[warp * 8 + 2 * t] = make_float2(lm[0], ls[0]);
+      lred[warp * 8 + 2 * t + 1] = make_float2(lm[1], ls[1]);
+    }
   }
   __syncthreads();
   if (threadIdx.x < (unsigned)M) {
@@ -555,6 +597,11 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
     }
     if (b != 0ull)
       asm volatile("red.relaxed.gpu.global.max.u64 [%0], %1;" ::"l"(p.keys + m), "l"(b) : "memory");
+    if (p.logprob != nullptr) {  // this CTA's log-sum-exp partial, combined in CTA order below
+      float cm = -INFINITY, cs = 0.f;
+      for (int w = 0; w < kWarps; ++w) lse_merge(cm, cs, lred[w * 8 + m].x, lred[w * 8 + m].y);
+      p.lse[(int64_t)blockIdx.x * 8 + m] = make_float2(cm, cs);
+    }
   }
   // Count the finished CTAs with an acquire-release add: the barrier orders this
   // CTA's key updates before thread 0's release, and the last CTA's acquire
@@ -574,6 +621,21 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
       asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p.keys + threadIdx.x), "l"(0ull) : "memory");
       p.argmax[threadIdx.x] =
           key == 0ull ? 0 : (int32_t)(0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFull));
+      if (p.logprob != nullptr) {
+        float cm = -INFINITY, cs = 0.f;
+        for (unsigned int b = 0; b < gridDim.x; ++b) {
+          float2 v;
+          asm volatile("ld.relaxed.gpu.global.v2.f32 {%0, %1}, [%2];"
+                       : "=f"(v.x), "=f"(v.y)
+                       : "l"(p.lse + (int64_t)b * 8 + threadIdx.x)
+                       : "memory");
+          lse_merge(cm, cs, v.x, v.y);
+        }
+        // the winning logit back from its key (inverse of the order-preserving map)
+        const uint32_t o = (uint32_t)(key >> 32);
+        const float ymax = __uint_as_float((o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o);
+        p.logprob[threadIdx.x] = key == 0ull ? __int_as_float(0x7FC00000) : ymax - (cm + logf(cs));
+      }
     }
     if (threadIdx.x == 0)
       asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p.counter), "r"(0u) : "memory");
@@ -611,7 +673,7 @@ Layout layout_for(int warps, int m, int nchunks) {
   off += (16 + 16 * warps + 8 + 16) * sizeof(float);
   off = (off + 15) & ~(size_t)15;
   l.off_kred = (uint32_t)off;
-  off += (size_t)warps * 8 * sizeof(unsigned long long);
+  off += (size_t)warps * 8 * sizeof(unsigned long long) + (size_t)warps * 8 * sizeof(float2);
   off = (off + 1023) & ~(size_t)1023;
   l.off_ring = (uint32_t)off;
   off += (size_t)warps * kRing * kStageBytes;
@@ -625,7 +687,8 @@ Layout layout_for(int warps, int m, int nchunks) {
 
 int launch_gemv(const w4a16_act_segment* seg, int nseg, int m, const nvfp4_weight* w, void* y,
                 int y_dtype, int64_t ldy, bool want_argmax, int32_t* argmax, void* workspace,
-                int32_t* dev_status, cudaStream_t stream) {
+                int32_t* dev_status, cudaStream_t stream, float* logprob, const int32_t* mask,
+                int64_t ld_mask) {
   GemvParams p{};
   for (int s = 0; s < 2; ++s) {
     p.x[s] = s < nseg ? reinterpret_cast<const __nv_bfloat16*>(seg[s].x) : nullptr;
@@ -647,6 +710,10 @@ int launch_gemv(const w4a16_act_segment* seg, int nseg, int m, const nvfp4_weigh
     p.keys = reinterpret_cast<unsigned long long*>(workspace);
     p.counter = reinterpret_cast<unsigned int*>(reinterpret_cast<char*>(workspace) + 64);
     p.argmax = argmax;
+    p.logprob = logprob;
+    p.mask = mask;
+    p.ld_mask = ld_mask;
+    p.lse = reinterpret_cast<float2*>(reinterpret_cast<char*>(workspace) + 128);
   }
   p.dev_status = dev_status;
   p.ntiles = nvfp4::cdiv(w->n, 16);
@@ -694,7 +761,8 @@ int launch_gemv(const w4a16_act_segment* seg, int nseg, int m, const nvfp4_weigh
   if (ks > 1 && warps / ks > 4) ks = warps / 4;
   p.ks = ks;
   const int64_t ngroups = nvfp4::cdiv(p.ntiles, warps / ks);
-  const int64_t grid = ngroups < slots ? ngroups : slots;
+  int64_t grid = ngroups < slots ? ngroups : slots;
+  if (grid > W4A16_GEMV_MAX_CTAS) grid = W4A16_GEMV_MAX_CTAS;  // bound of the log-prob workspace
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
   cfg.blockDim = dim3(warps * 32);

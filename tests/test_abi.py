@@ -107,6 +107,27 @@ def test_gemv_argmax_needs_workspace(L):
     assert f(seg, 1, 1, ctypes.byref(w), 0x6002, 256, 0x7000, ctypes.byref(ex)) == 3
 
 
+def test_gemv_argmax_ex_argument_checks(L):
+    import nvfp4_speculative_draft_gb300 as nd
+    w = _weight(nd)                      # n = 256 -> 8 mask words
+    seg = (nd._Segment * 1)(_seg(nd))
+    f = L.w4a16_gemv_argmax_ex
+    ok = nd._Exec(None, 0x10000, nd.ARGMAX_EX_WS_BYTES, None)
+    small = nd._Exec(None, 0x10000, nd.ARGMAX_WS_BYTES, None)
+    assert f(seg, 1, 1, ctypes.byref(w), 0x6000, 256, 0x7000, 0x7100, 0x7200, 8,
+             ctypes.byref(small)) == 4
+    assert f(seg, 1, 1, ctypes.byref(w), 0x6000, 256, None, 0x7100, 0x7200, 8,
+             ctypes.byref(ok)) == 1
+    assert f(seg, 1, 1, ctypes.byref(w), 0x6000, 256, 0x7000, 0x7100, 0x7200, 7,
+             ctypes.byref(ok)) == 2
+    assert f(seg, 1, 1, ctypes.byref(w), 0x6000, 256, 0x7000, 0x7102, 0x7200, 8,
+             ctypes.byref(ok)) == 3
+    assert f(seg, 1, 1, ctypes.byref(w), 0x6000, 256, 0x7000, 0x7100, 0x7201, 8,
+             ctypes.byref(ok)) == 3
+    assert f(seg, 1, 9, ctypes.byref(w), 0x6000, 256, 0x7000, 0x7100, 0x7200, 8,
+             ctypes.byref(ok)) == 2
+
+
 def test_gemm_argument_checks(L):
     import nvfp4_speculative_draft_gb300 as nd
     ex = nd._Exec(None, None, 0, None)

@@ -76,6 +76,24 @@ def check_logits_and_argmax(lg, idx, y, sabs):
             assert y[r, i] >= y[r, j] - tol[r, j] - tol[r, i]
 
 
+def half_mask(m_rows, n, seed):
+    """Grammar bitmask words [m, ceil(n/32)] with about half the tokens allowed."""
+    rng = np.random.default_rng(seed)
+    return rng.integers(-2 ** 31, 2 ** 31, size=(m_rows, (n + 31) // 32), dtype=np.int64).astype(np.int32)
+
+
+def mask_bits(words, n):
+    b = words.view(np.uint32)
+    j = np.arange(n)
+    return ((b[j // 32] >> (j % 32).astype(np.uint32)) & 1).astype(bool)
+
+
+def lse64(v):
+    v = np.asarray(v, dtype=np.float64)
+    mx = v.max()
+    return mx + np.log(np.exp(v - mx).sum())
+
+
 def test_tiny_config(dev):
     m = nd()
     case = workloads.tiny()
@@ -124,6 +142,21 @@ def test_propose_config_full_width(dev):
     torch.cuda.synchronize()
     y, sabs = par_gemv(workloads.bits(x[:1]), pk, sc, g)
     check_logits_and_argmax(logits.cpu().numpy(), idx.cpu().numpy(), y, sabs)
+    lg1 = logits.cpu().numpy()
+    # grammar mask + top-1 log-probability at full width (M=1 against the exact
+    # logits, the larger batches against the GPU's own logits)
+    mask = half_mask(8, 151936, seed=21)
+    _, idx, lp = m.w4a16_gemv_argmax_ex([(x[:1], None)], wq, mask=torch.from_numpy(mask[:1]).to(dev),
+                                        logits=False)
+    torch.cuda.synchronize()
+    i = int(idx[0])
+    assert i == oracle.argmax_masked(lg1[0].astype(np.float64), mask[0])
+    j = oracle.argmax_masked(y[0], mask[0])
+    tol = TOL_REL * sabs[0] + TOL_ABS
+    assert y[0, i] >= y[0, j] - tol[i] - tol[j]
+    allowed = mask_bits(mask[0], 151936)
+    lp_ref = oracle.top1_logprob(y[0], j, mask[0])
+    assert abs(float(lp[0]) - lp_ref) <= tol[i] + tol[allowed].max() + 1e-5 * (1 + abs(float(lg1[0, i])))
     for mm in (2, 4, 8):
         logits, idx = m.w4a16_gemv_argmax([(x[:mm].contiguous(), None)], wq)
         torch.cuda.synchronize()
@@ -133,6 +166,15 @@ def test_propose_config_full_width(dev):
         assert np.all(err <= TOL_REL * ss + TOL_ABS)
         for r in range(mm):
             assert int(idx[r]) == oracle.argmax(lg[r].astype(np.float64))
+        _, idx, lp = m.w4a16_gemv_argmax_ex([(x[:mm].contiguous(), None)], wq,
+                                            mask=torch.from_numpy(mask[:mm]).to(dev), logits=False)
+        torch.cuda.synchronize()
+        for r in range(mm):
+            i = int(idx[r])
+            assert i == oracle.argmax_masked(lg[r].astype(np.float64), mask[r])
+            allowed = mask_bits(mask[r], 151936)
+            own = float(lg[r, i]) - lse64(lg[r, allowed])
+            assert abs(float(lp[r]) - own) <= 1e-5 * (1 + abs(float(lg[r, i])))
 
 
 @pytest.mark.parametrize("mm", [1, 4, 8])
