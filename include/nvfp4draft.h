@@ -66,6 +66,16 @@ extern "C" {
  * (keys + counter, then one (max, sum) pair per CTA and batch row). */
 #define W4A16_GEMV_MAX_CTAS 1024
 #define W4A16_ARGMAX_EX_WS_BYTES (128 + W4A16_GEMV_MAX_CTAS * 8 * 8)
+/* Optional larger GEMV workspace: with at least W4A16_GEMV_WS_BYTES(m, k)
+ * bytes (16-byte aligned) and m >= 2, the GEMV calls normalise the
+ * activations once in a small grid of their own (one CTA per batch row) and
+ * every GEMV CTA copies the result, instead of each CTA normalising all rows
+ * itself; results are bit-identical either way.  Layout: the
+ * argmax / log-prob area above, then the per-row scale carriers at
+ * W4A16_GEMV_PREP_OFFSET and the FP16 fragments 256 bytes further on. */
+#define W4A16_GEMV_PREP_OFFSET 65664
+#define W4A16_GEMV_WS_BYTES(m, k) \
+  ((size_t)W4A16_GEMV_PREP_OFFSET + 256 + ((size_t)(k) + 255) / 256 * 512 * (size_t)(m))
 /* Workspace of nvfp4_quantize when its absmax output is NULL. */
 #define NVFP4_QUANTIZE_WS_BYTES 16
 /* Optional workspace of w4a16_gemm that enables its FP16 staging path. */
@@ -140,7 +150,8 @@ int nvfp4_quantize(const void *w_bf16, int64_t n, int64_t k, uint8_t *packed,
  *   w             host struct describing the weight; w->k <= W4A16_GEMV_MAX_K.
  *   y             device [m, ldy] of y_dtype (F32 or BF16, round-to-nearest-even),
  *                 ldy >= w->n.
- * Workspace: none.
+ * Workspace: none required; with W4A16_GEMV_WS_BYTES(m, w->k) bytes the
+ * activations are prepared once for all CTAs (same results either way).
  */
 int w4a16_gemv(const w4a16_act_segment *seg, int nseg, int m, const nvfp4_weight *w,
                void *y, int y_dtype, int64_t ldy, const nvfp4_exec *ex);

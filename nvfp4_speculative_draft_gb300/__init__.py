@@ -34,6 +34,12 @@ GEMV_MAX_K = 16384
 ARGMAX_WS_BYTES = 128
 GEMV_MAX_CTAS = 1024
 ARGMAX_EX_WS_BYTES = 128 + GEMV_MAX_CTAS * 8 * 8
+GEMV_PREP_OFFSET = ARGMAX_EX_WS_BYTES
+
+
+def gemv_workspace_bytes(m: int, k: int) -> int:
+    """W4A16_GEMV_WS_BYTES: argmax / log-prob area plus prepared activations."""
+    return GEMV_PREP_OFFSET + 256 + (k + 255) // 256 * 512 * m
 QUANTIZE_WS_BYTES = 16
 EXPORTED = ("nvfp4_quantize", "w4a16_gemv", "w4a16_gemv_argmax", "w4a16_gemv_argmax_ex",
             "w4a16_gemm")
@@ -121,13 +127,15 @@ _WS = {}
 
 
 def argmax_workspace(device) -> torch.Tensor:
-    """A zeroed argmax workspace per device (each completed call re-zeroes it),
-    large enough for :func:`w4a16_gemv_argmax_ex`.  Calls on concurrent
-    streams must pass their own workspace instead."""
+    """A zeroed GEMV workspace per device (each completed call re-zeroes its
+    argmax area), large enough for every GEMV call at any m <= 8 and k <= 16384
+    (argmax, log-probability and the once-per-call activation preparation).
+    Calls on concurrent streams must pass their own workspace instead."""
     device = torch.device(device)
     key = ("argmax", device.index)
     if key not in _WS:
-        _WS[key] = torch.zeros(ARGMAX_EX_WS_BYTES, dtype=torch.uint8, device=device)
+        _WS[key] = torch.zeros(gemv_workspace_bytes(GEMV_MAX_M, GEMV_MAX_K), dtype=torch.uint8,
+                               device=device)
     return _WS[key]
 
 
@@ -175,13 +183,18 @@ def _segments(segments: Sequence) -> tuple:
 
 def w4a16_gemv(segments: Sequence, weight: Nvfp4Weight, out_dtype=torch.float32,
                out: Optional[torch.Tensor] = None, stream=None,
-               dev_status: Optional[torch.Tensor] = None) -> torch.Tensor:
+               dev_status: Optional[torch.Tensor] = None,
+               workspace: Optional[torch.Tensor] = None, prepare: bool = True) -> torch.Tensor:
+    """``prepare``: use the per-device workspace (or ``workspace``) so the
+    activations are normalised once per call rather than in every CTA."""
     segs, m = _segments(segments)
     if out is None:
         out = torch.empty((m, weight.n), dtype=out_dtype, device=weight.packed.device)
     dt = DTYPE_F32 if out.dtype == torch.float32 else DTYPE_BF16
     assert out.dtype in (torch.float32, torch.bfloat16) and out.stride(1) == 1
-    ex = _exec(stream, None, dev_status)
+    if workspace is None and prepare:
+        workspace = argmax_workspace(weight.packed.device)
+    ex = _exec(stream, workspace, dev_status)
     w = weight.c()
     rc = load().w4a16_gemv(segs, len(segments), m, ctypes.byref(w), out.data_ptr(), dt,
                            out.stride(0), ctypes.byref(ex))

@@ -161,8 +161,9 @@ int w4a16_gemv(const w4a16_act_segment* seg, int nseg, int m, const nvfp4_weight
   if (ldy < w->n) return NVFP4_ERR_SHAPE;
   const uintptr_t ya = reinterpret_cast<uintptr_t>(y);
   if ((y_dtype == NVFP4_DTYPE_F32 && (ya & 3u)) || (ya & 1u)) return NVFP4_ERR_ALIGN;
-  return launch_gemv(seg, nseg, m, w, y, y_dtype, ldy, false, nullptr, nullptr, status_of(ex),
-                     stream_of(ex));
+  return launch_gemv(seg, nseg, m, w, y, y_dtype, ldy, false, nullptr,
+                     ex != nullptr ? ex->workspace : nullptr, ex != nullptr ? ex->workspace_bytes : 0,
+                     status_of(ex), stream_of(ex));
 }
 
 int w4a16_gemv_argmax(const w4a16_act_segment* seg, int nseg, int m, const nvfp4_weight* w,
@@ -181,7 +182,7 @@ int w4a16_gemv_argmax(const w4a16_act_segment* seg, int nseg, int m, const nvfp4
       !aligned16(ex->workspace))
     return NVFP4_ERR_WORKSPACE;
   return launch_gemv(seg, nseg, m, w, logits, NVFP4_DTYPE_F32, ld_logits, true, argmax,
-                     ex->workspace, status_of(ex), stream_of(ex));
+                     ex->workspace, ex->workspace_bytes, status_of(ex), stream_of(ex));
 }
 
 int w4a16_gemv_argmax_ex(const w4a16_act_segment* seg, int nseg, int m, const nvfp4_weight* w,
@@ -204,7 +205,8 @@ int w4a16_gemv_argmax_ex(const w4a16_act_segment* seg, int nseg, int m, const nv
       !aligned16(ex->workspace))
     return NVFP4_ERR_WORKSPACE;
   return launch_gemv(seg, nseg, m, w, logits, NVFP4_DTYPE_F32, ld_logits, true, argmax,
-                     ex->workspace, status_of(ex), stream_of(ex), logprob, mask, ld_mask);
+                     ex->workspace, ex->workspace_bytes, status_of(ex), stream_of(ex), logprob, mask,
+                     ld_mask);
 }
 
 int w4a16_gemm(const void* a_bf16, int64_t m, int64_t lda, const nvfp4_weight* w, void* c_bf16,

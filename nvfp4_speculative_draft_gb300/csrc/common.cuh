@@ -64,7 +64,7 @@ int launch_quantize(const void* w, int64_t n, int64_t k, uint8_t* packed, uint8_
                     cudaStream_t stream);
 int launch_gemv(const w4a16_act_segment* seg, int nseg, int m, const nvfp4_weight* w,
                 void* y, int y_dtype, int64_t ldy, bool want_argmax, int32_t* argmax,
-                void* workspace, int32_t* dev_status, cudaStream_t stream,
+                void* workspace, size_t workspace_bytes, int32_t* dev_status, cudaStream_t stream,
                 float* logprob = nullptr, const int32_t* mask = nullptr, int64_t ld_mask = 0);
 int launch_gemm(const void* a, int64_t m, int64_t lda, const nvfp4_weight* w, void* c,
                 int64_t ldc, void* workspace, size_t workspace_bytes, int32_t* dev_status,

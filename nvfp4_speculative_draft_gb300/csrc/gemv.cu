@@ -51,7 +51,7 @@ constexpr int kStageBytes = 16 * 64 * kItem;
 // rings measured no faster).
 __host__ __device__ constexpr int ring_stages(int, int) { return 2; }
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
-constexpr int kL2Prefetch = 8;    // items per warp pulled into L2 while the previous call ends
+constexpr int kL2Prefetch = 4;    // items per warp pulled into L2 while the previous call ends
 
 struct GemvParams {
   const __nv_bfloat16* x[2];
@@ -76,6 +76,8 @@ struct GemvParams {
   int64_t ld_mask;
   int32_t* dev_status;
   int ks;          // warps sharing one 16-row tile (split K)
+  const uint2* frag_src;          // fragments prepared by act_prep_kernel, or null
+  const unsigned int* rowmax_src; // their per-row scale carriers [8]
   int64_t ntiles;  // ceil(n / 16)
   int nchunks;     // ceil(k / 128)
   // shared-memory carve-up (bytes from the 1 KB-aligned base)
@@ -125,6 +127,13 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
 __device__ __forceinline__ uint32_t f16x2_mul(uint32_t a, uint32_t b) {
   uint32_t d;
   asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
@@ -144,10 +153,12 @@ __device__ __forceinline__ void mma_f16_16816(float (&c)[4], uint32_t a0, uint32
 // Two E4M3 block scales (low byte first) -> F16 (exact: E4M3 values are F16
 // normals), each replicated into both halves of an f16x2.
 __device__ __forceinline__ void decode_scales(uint32_t s2, uint32_t& lo, uint32_t& hi) {
-  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)s2, __NV_E4M3);
-  const uint32_t v = (uint32_t)h.x | ((uint32_t)h.y << 16);
-  lo = __byte_perm(v, 0, 0x1010);
-  hi = __byte_perm(v, 0, 0x3232);
+  // both halves of lo (hi) carry the first (second) scale: the broadcast is
+  // written as half moves, which the multiply can take as operand selects
+  asm("{\n .reg .b16 a, b;\n .reg .b32 v;\n cvt.rn.f16x2.e4m3x2 v, %2;\n mov.b32 {a, b}, v;\n"
+      " mov.b32 %0, {a, a};\n mov.b32 %1, {b, b};\n}"
+      : "=r"(lo), "=r"(hi)
+      : "h"((uint16_t)s2));
 }
 
 // The 8 E2M1 codes of word q -> 4 f16x2 (nibbles 0|1, 2|3, 4|5, 6|7; the even
@@ -203,7 +214,7 @@ __device__ __forceinline__ unsigned long long argmax_key(float v, uint32_t idx) 
 __device__ __forceinline__ void lse_merge(float& m, float& s, float om, float os) {
   const float nm = fmaxf(m, om);
   if (nm == -INFINITY) return;  // both empty
-  s = s * expf(m - nm) + os * expf(om - nm);
+  s = s * __expf(m - nm) + os * __expf(om - nm);
   m = nm;
 }
 
@@ -228,113 +239,164 @@ __device__ __forceinline__ float row_scale_pow2(unsigned int maxbits, bool inver
 // uint2 at bfrag[q * 4M + L].  For the 8 activations at
 // kk = 128 c + 32 t + 8 w (+0..7):  MMA 8c+2w gets {a0,a4},{a1,a5};
 // MMA 8c+2w+1 gets {a2,a6},{a3,a7}.  Positions past k are zero.
+// Shared "small" area (floats): [0,16) inverse RMS per (row, segment);
+// [16,24) per-row scale exponent carrier (BF16 magnitude bits, see
+// row_scale_pow2); [24,26) max |gamma| per segment; [32,48) max |x| per
+// (row, segment); then per-(job, warp) partial sums of squares and maxima.
+constexpr int kSmallRowmax = 16, kSmallMaxg = 24, kSmallMaxx = 32, kSmallParts = 48;
+constexpr int kMaxJobs = 24;  // 8 rows x 2 segments + 2 gamma jobs, rounded up
+__host__ __device__ constexpr int small_floats(int warps) { return kSmallParts + 2 * kMaxJobs * warps; }
+
+// Kept out of line: the prologue's registers then do not compete with the
+// main loop's (which hold the first ring stages' scales across it).
+// Rows r0 .. r0+nrows-1 of the batch; bfrag may be shared or global memory
+// (generic addresses), rowmax_out receives the rows' scale carriers too.
 template <int M, int WARPS>
-__device__ void build_fragments(const GemvParams& p, uint2* bfrag, float* rms) {
+__device__ __noinline__ void build_fragments(const GemvParams& p, uint2* bfrag, float* small, int r0,
+                                             int nrows, unsigned int* rowmax_out) {
   constexpr int BSTRIDE = 4 * M;
   constexpr int kWarps = WARPS, kThreads = WARPS * 32;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  // 1. inverse RMS per (row, segment) job.  The CTA's warps split each job's
-  //    k range (all 16 warps for a single job), four 16-byte loads in flight
-  //    per lane; per-(job, warp) partial sums are combined in a fixed order,
-  //    so the result does not depend on timing.
-  float* part = rms + 16;  // [16 jobs][kWarps]
-  unsigned int* rowmax = reinterpret_cast<unsigned int*>(part + 16 * kWarps);  // [8]
-  if (tid < 8) rowmax[tid] = 0u;  // ordered before its use by the barriers below
-  const int J = M * p.nseg;
+  float* rms = small;
+  unsigned int* rowmax = reinterpret_cast<unsigned int*>(small + kSmallRowmax);
+  float* maxg = small + kSmallMaxg;
+  float* maxx = small + kSmallMaxx;
+  float* part_ss = small + kSmallParts;                                          // [job][warp]
+  unsigned int* part_mx = reinterpret_cast<unsigned int*>(part_ss + kMaxJobs * kWarps);
+  // 1. statistics.  Jobs 0 .. M*nseg-1: row r = job / nseg, segment s: sum of
+  //    squares (RMSNorm segments) and the largest |x| (BF16 magnitude bits
+  //    order like the values).  Jobs M*nseg + s: the largest |gamma_s|.  The
+  //    CTA's warps split each job's k range; partials are combined in a fixed
+  //    order, so the result does not depend on timing.
+  const int JR = nrows * p.nseg, J = JR + p.nseg;
   const int wpj = J >= kWarps ? 1 : kWarps / J;  // warps per job
   const int jpp = kWarps / wpj;                  // jobs per pass
   for (int j0 = 0; j0 < J; j0 += jpp) {
     const int job = j0 + warp / wpj, wj = warp % wpj;
     if (job < J) {
-      const int r = job / p.nseg, s = job % p.nseg;
+      const int s = job < JR ? job % p.nseg : job - JR;
+      const bool is_gamma = job >= JR;
+      const __nv_bfloat16* src =
+          is_gamma ? p.gamma[s] : p.x[s] + (int64_t)(r0 + job / p.nseg) * p.ld[s];
+      const bool want_ss = !is_gamma && p.gamma[s] != nullptr;
       float ss = 0.0f;
-      if (p.gamma[s] != nullptr) {
-        const __nv_bfloat16* xr = p.x[s] + (int64_t)r * p.ld[s];
+      uint32_t mx = 0u;
+      if (src != nullptr) {
 #pragma unroll 4
-        for (int64_t i = (int64_t)(wj * 32 + lane) * 8; i < p.kseg[s]; i += (int64_t)wpj * 256) {
-          if (!NVFP4_GUARD(r < M && s < p.nseg && i + 8 <= p.kseg[s], 1, p.dev_status)) continue;
-          const uint4 v = *reinterpret_cast<const uint4*>(xr + i);
+        for (int i = (wj * 32 + lane) * 8; i < (int)p.kseg[s]; i += wpj * 256) {
+          if (!NVFP4_GUARD(s < p.nseg && i + 8 <= p.kseg[s], 1, p.dev_status)) continue;
+          const uint4 v = *reinterpret_cast<const uint4*>(src + i);
           const uint32_t u[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            const float a = __uint_as_float(u[j] << 16), b = __uint_as_float(u[j] & 0xFFFF0000u);
-            ss = fmaf(a, a, ss);
-            ss = fmaf(b, b, ss);
+            mx = __vmaxu2(mx, u[j] & 0x7FFF7FFFu);
+            if (want_ss) {
+              const float a = __uint_as_float(u[j] << 16), b = __uint_as_float(u[j] & 0xFFFF0000u);
+              ss = fmaf(a, a, ss);
+              ss = fmaf(b, b, ss);
+            }
           }
         }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
       }
-      if (lane == 0) part[job * kWarps + wj] = ss;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
+      mx = __reduce_max_sync(0xFFFFFFFFu, max(mx & 0xFFFFu, mx >> 16));
+      if (lane == 0) {
+        part_ss[job * kWarps + wj] = ss;
+        part_mx[job * kWarps + wj] = mx;
+      }
     }
   }
   __syncthreads();
   if (tid < J) {
-    const int s = tid % p.nseg;
+    const int s = tid < JR ? tid % p.nseg : tid - JR;
     float ss = 0.0f;
-    for (int w = 0; w < wpj; ++w) ss += part[tid * kWarps + w];
-    rms[tid] = p.gamma[s] == nullptr ? 1.0f : 1.0f / sqrtf(ss / (float)p.kseg[s] + p.eps[s]);
+    unsigned int mx = 0u;
+    for (int w = 0; w < wpj; ++w) {
+      ss += part_ss[tid * kWarps + w];
+      mx = max(mx, part_mx[tid * kWarps + w]);
+    }
+    if (tid < JR) {
+      rms[tid] = p.gamma[s] == nullptr ? 1.0f : 1.0f / sqrtf(ss / (float)p.kseg[s] + p.eps[s]);
+      maxx[tid] = __uint_as_float(mx << 16);
+    } else {
+      maxg[s] = __uint_as_float(mx << 16);
+    }
   }
   __syncthreads();
-  // 2. normalised BF16 activations into the fragment slots.  The 8 activations
-  //    at kk = 128c + 32t + 8w of row m fill MMA 8c+2w (elements 0..3) and MMA
-  //    8c+2w+1 (elements 4..7) of lane 4m + t.  Positions past k are zero.
-  //    The largest magnitude of each row is collected on the way (the BF16
-  //    magnitude bits order like the values).
-  const int64_t gpr = (int64_t)p.nchunks * (kChunk / 8);  // 8-element groups per row
-#pragma unroll 4
-  for (int64_t gi = tid; gi < (int64_t)M * gpr; gi += kThreads) {
-    const int r = (int)(gi / gpr);
-    const int64_t kk = (gi % gpr) * 8;
-    uint32_t a[4] = {0u, 0u, 0u, 0u};  // bf16 pairs (a0,a1),(a2,a3),(a4,a5),(a6,a7)
-    const int s = (p.nseg == 2 && kk >= p.kseg[0]) ? 1 : 0;
-    const int64_t ko = kk - (s ? p.kseg[0] : 0);
-    if (kk < p.k && NVFP4_GUARD(r < M && ko >= 0 && ko + 8 <= p.kseg[s], 2, p.dev_status)) {
-      const uint4 v = *reinterpret_cast<const uint4*>(p.x[s] + (int64_t)r * p.ld[s] + ko);
-      a[0] = v.x; a[1] = v.y; a[2] = v.z; a[3] = v.w;
-      if (p.gamma[s] != nullptr) {
-        const uint4 gv = *reinterpret_cast<const uint4*>(p.gamma[s] + ko);
-        const uint32_t gg[4] = {gv.x, gv.y, gv.z, gv.w};
-        const float rr = rms[r * p.nseg + s];
+  // Per-row power of two 2^e from an upper bound B of the row's normalised
+  // magnitudes (|bf16(x r gamma)| <= max|x| r max|gamma| (1 + 2^-7)): B 2^e
+  // lies in [2^14, 2^15), so every activation converts to FP16 without
+  // overflow, and exactly unless it is below 2^-29 B.
+  if (tid < nrows) {
+    float bound = 0.0f;
+    for (int s = 0; s < p.nseg; ++s) {
+      const int j = tid * p.nseg + s;
+      const float b = p.gamma[s] == nullptr ? maxx[j] : maxx[j] * rms[j] * maxg[s] * (1.0f + 0.0078125f);
+      bound = fmaxf(bound, b);
+    }
+    const unsigned int carrier = __float_as_uint(bound) >> 16;  // carries the bound's exponent
+    rowmax[r0 + tid] = carrier;
+    if (rowmax_out != nullptr) rowmax_out[r0 + tid] = carrier;
+  }
+  __syncthreads();
+  // 2. normalised, scaled FP16 activations into the fragment slots.  The 8
+  //    activations at kk = 128c + 32t + 8w of row m fill MMA 8c+2w (elements
+  //    0..3) and MMA 8c+2w+1 (elements 4..7) of lane 4m + t.  Positions past k
+  //    are zero.
+  const int gpr = p.nchunks * (kChunk / 8);  // 8-element groups per row
+  for (int r = r0; r < r0 + nrows; ++r) {
+    const float sc = row_scale_pow2(rowmax[r], false);
+#pragma unroll 2
+    for (int q = tid; q < gpr; q += kThreads) {
+      const int kk = q * 8;
+      uint32_t a[4] = {0u, 0u, 0u, 0u};  // bf16 pairs (a0,a1),(a2,a3),(a4,a5),(a6,a7)
+      const int s = (p.nseg == 2 && kk >= p.kseg[0]) ? 1 : 0;
+      const int ko = kk - (s ? (int)p.kseg[0] : 0);
+      if (kk < p.k && NVFP4_GUARD(ko >= 0 && ko + 8 <= p.kseg[s], 2, p.dev_status)) {
+        const uint4 v = *reinterpret_cast<const uint4*>(p.x[s] + (int64_t)r * p.ld[s] + ko);
+        a[0] = v.x; a[1] = v.y; a[2] = v.z; a[3] = v.w;
+        if (p.gamma[s] != nullptr) {
+          const uint4 gv = *reinterpret_cast<const uint4*>(p.gamma[s] + ko);
+          const uint32_t gg[4] = {gv.x, gv.y, gv.z, gv.w};
+          const float rr = rms[(r - r0) * p.nseg + s];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float lo = __uint_as_float(a[j] << 16) * rr * __uint_as_float(gg[j] << 16);
-          const float hi =
-              __uint_as_float(a[j] & 0xFFFF0000u) * rr * __uint_as_float(gg[j] & 0xFFFF0000u);
-          a[j] = pack_bf16x2(lo, hi);
+          for (int j = 0; j < 4; ++j) {
+            const float lo = __uint_as_float(a[j] << 16) * rr * __uint_as_float(gg[j] << 16);
+            const float hi =
+                __uint_as_float(a[j] & 0xFFFF0000u) * rr * __uint_as_float(gg[j] & 0xFFFF0000u);
+            a[j] = pack_bf16x2(lo, hi);
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {  // BF16 -> FP16, times 2^e (exact)
+          const __half2 h = __floats2half2_rn(__uint_as_float(a[j] << 16) * sc,
+                                              __uint_as_float(a[j] & 0xFFFF0000u) * sc);
+          a[j] = *reinterpret_cast<const uint32_t*>(&h);
         }
       }
-      const uint32_t mx = __vmaxu2(__vmaxu2(a[0] & 0x7FFF7FFFu, a[1] & 0x7FFF7FFFu),
-                                   __vmaxu2(a[2] & 0x7FFF7FFFu, a[3] & 0x7FFF7FFFu));
-      const uint32_t m1 = max(mx & 0xFFFFu, mx >> 16);
-      if (m1 != 0u) atomicMax(rowmax + r, m1);
+      const int c = kk / kChunk, t = (kk % kChunk) / 32, w = (kk % 32) / 8;
+      const int L = 4 * r + t;
+      if (!NVFP4_GUARD((8 * c + 2 * w + 1) * BSTRIDE + L < p.nchunks * 8 * BSTRIDE && L < BSTRIDE, 3,
+                       p.dev_status))
+        continue;
+      bfrag[(8 * c + 2 * w) * BSTRIDE + L] = make_uint2(a[0], a[1]);
+      bfrag[(8 * c + 2 * w + 1) * BSTRIDE + L] = make_uint2(a[2], a[3]);
     }
-    const int c = (int)(kk / kChunk), t = (int)((kk % kChunk) / 32), w = (int)((kk % 32) / 8);
-    const int L = 4 * r + t;
-    if (!NVFP4_GUARD((int64_t)(8 * c + 2 * w + 1) * BSTRIDE + L < (int64_t)p.nchunks * 8 * BSTRIDE &&
-                         L < BSTRIDE, 3, p.dev_status))
-      continue;
-    bfrag[(int64_t)(8 * c + 2 * w) * BSTRIDE + L] = make_uint2(a[0], a[1]);
-    bfrag[(int64_t)(8 * c + 2 * w + 1) * BSTRIDE + L] = make_uint2(a[2], a[3]);
   }
-  __syncthreads();
-  // 3. BF16 -> FP16 in place, times a per-row power of two 2^e that puts the
-  //    row's largest magnitude in [2^14, 2^15): every BF16 activation within
-  //    2^-31 of it then converts exactly (8 significant bits, FP16 normal range).
-  const int64_t slots = (int64_t)p.nchunks * 8 * BSTRIDE;
-  for (int64_t i = tid; i < slots; i += kThreads) {
-    const float sc = row_scale_pow2(rowmax[(int)(i % BSTRIDE) / 4], false);
-    uint2 v = bfrag[i];
-    const uint32_t u[2] = {v.x, v.y};
-    uint32_t o[2];
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      const __half2 h = __floats2half2_rn(__uint_as_float(u[j] << 16) * sc,
-                                          __uint_as_float(u[j] & 0xFFFF0000u) * sc);
-      o[j] = *reinterpret_cast<const uint32_t*>(&h);
-    }
-    bfrag[i] = make_uint2(o[0], o[1]);
-  }
+}
+
+// One CTA per batch row: normalise, scale and convert the row's activations
+// once into the fragment layout in global memory, for every GEMV CTA to copy.
+// It waits for the previous grid before reading x and lets the GEMV start
+// right after (the GEMV reads the fragments only after its own wait).
+template <int M>
+__global__ void __launch_bounds__(512) act_prep_kernel(const __grid_constant__ GemvParams p, uint2* frag,
+                                                       unsigned int* rowmax) {
+  __shared__ __align__(16) float small[small_floats(16)];
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  build_fragments<M, 16>(p, frag, small, (int)blockIdx.x, 1, rowmax);
 }
 
 // Named barriers over the `count` threads of one tile group: the split-K
@@ -388,10 +450,14 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
   const int cmax = (int)((p.k - 32 * t + kChunk - 1) / kChunk);
   bool alive = true;  // false once a wait ran out
 
+  const bool prepped = p.frag_src != nullptr;
+  const uint32_t fbar = base + p.off_bar + (uint32_t)kWarps * (kRing * 8);  // fragment copy
   if (lane == 0) {
     for (int i = 0; i < kRing; ++i) mbar_init(bars + 8 * i, 1);
+    if (threadIdx.x == 0) mbar_init(fbar, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
+  if (prepped) __syncthreads();  // fbar initialised before any thread waits on it
   __syncwarp();
 
   // load cursor over (tile, item); scale row pointers change once per tile
@@ -444,19 +510,41 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
       if (++pc == L) { pc = 0; ++pt; }
     }
   }
+  // With prepared fragments the previous grid is act_prep_kernel, which let
+  // this grid start only after its own predecessor had finished: the weights
+  // are final, so the first ring stages may load before the wait.
+  if (prepped) {
+#pragma unroll
+    for (int i = 0; i < kRing; ++i)
+      if (i < total) issue(i);
+  }
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
-  // start streaming before the activation prologue
+  if (prepped) {
+    // one bulk copy of the prepared fragments and row-scale carriers
+    if (threadIdx.x == 0) {
+      const uint32_t fbytes = (uint32_t)p.nchunks * 8u * BSTRIDE * 8u;
+      mbar_arrive_expect_tx(fbar, fbytes + 32u);
+      const uint32_t dst = base;  // bfrag
+      for (uint32_t off = 0; off < fbytes; off += 32768u) {
+        const uint32_t n = fbytes - off < 32768u ? fbytes - off : 32768u;
+        bulk_copy_g2s(dst + off, reinterpret_cast<const char*>(p.frag_src) + off, n, fbar);
+      }
+      bulk_copy_g2s(base + p.off_small + kSmallRowmax * 4u, p.rowmax_src, 32u, fbar);
+    }
+    if (!mbar_wait(fbar, 0u, p.dev_status)) alive = false;
+  } else {
+    // start streaming before the activation prologue
 #pragma unroll
-  for (int i = 0; i < kRing; ++i)
-    if (i < total) issue(i);
-
-  if (n_iter > 0 || blockIdx.x == 0) build_fragments<M, WARPS>(p, bfrag, rms);
+    for (int i = 0; i < kRing; ++i)
+      if (i < total) issue(i);
+    if (n_iter > 0 || blockIdx.x == 0) build_fragments<M, WARPS>(p, bfrag, rms, 0, M, nullptr);
+  }
   __syncthreads();
 
   const float gsc = __ldg(p.gscale);
   // inverse activation scales of this lane's two batch columns (2t, 2t+1)
-  const unsigned int* rowmax = reinterpret_cast<const unsigned int*>(rms + 16 + 16 * kWarps);
+  const unsigned int* rowmax = reinterpret_cast<const unsigned int*>(rms + kSmallRowmax);
   const float inv0 = row_scale_pow2(rowmax[min(2 * t, M - 1)], true);
   const float inv1 = row_scale_pow2(rowmax[min(2 * t + 1, M - 1)], true);
   const uint2* bbase = bfrag + (lane % BSTRIDE);
@@ -464,6 +552,20 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
   float lm[2] = {-INFINITY, -INFINITY}, ls[2] = {0.f, 0.f};  // log-sum-exp (max, sum)
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
   int ct = 0, cc = 0;  // compute cursor
+
+  // Grammar mask: the 16 rows of a tile share one 32-bit mask word per batch
+  // column; the consumer warp loads the next tile's words during this tile.
+  uint32_t mword[2] = {0xFFFFFFFFu, 0xFFFFFFFFu};
+  auto load_mask = [&](int it) {
+    if (p.mask == nullptr) return;
+    const int64_t tile = ((int64_t)blockIdx.x + (int64_t)it * gridDim.x) * tpc + slot;
+    if (it >= n_iter || tile >= p.ntiles) return;
+#pragma unroll
+    for (int e = 0; e < 2; ++e)
+      mword[e] = __ldg(reinterpret_cast<const uint32_t*>(p.mask) +
+                       min(2 * t + e, M - 1) * p.ld_mask + (tile >> 1));
+  };
+  if (kpart == 0) load_mask(0);
 
   auto epilogue = [&](int it) {
     const int64_t tile = ((int64_t)blockIdx.x + (int64_t)it * gridDim.x) * tpc + slot;
@@ -502,26 +604,22 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
             else
               reinterpret_cast<__nv_bfloat16*>(p.y)[mm * p.ldy + rows[h]] = __float2bfloat16_rn(v);
           }
-          if (p.keys != nullptr) {
-            const bool allowed =
-                p.mask == nullptr ||
-                ((__ldg(p.mask + mm * p.ld_mask + (rows[h] >> 5)) >> (rows[h] & 31)) & 1);
-            if (allowed) {
-              const unsigned long long key = argmax_key(v, (uint32_t)rows[h]);
-              best[e] = key > best[e] ? key : best[e];
-              if (p.logprob != nullptr) {  // online log-sum-exp over the allowed logits
-                if (v > lm[e]) {
-                  ls[e] = ls[e] * expf(lm[e] - v) + 1.0f;
-                  lm[e] = v;
-                } else {
-                  ls[e] += expf(v - lm[e]);
-                }
+          if (p.keys != nullptr && ((mword[e] >> (((int)(tile & 1) << 4) + g + 8 * h)) & 1u)) {
+            const unsigned long long key = argmax_key(v, (uint32_t)rows[h]);
+            best[e] = key > best[e] ? key : best[e];
+            if (p.logprob != nullptr) {  // online log-sum-exp over the allowed logits
+              if (v > lm[e]) {
+                ls[e] = ls[e] * __expf(lm[e] - v) + 1.0f;
+                lm[e] = v;
+              } else {
+                ls[e] += __expf(v - lm[e]);
               }
             }
           }
         }
       }
     }
+    if (kpart == 0) load_mask(it + 1);
     acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
   };
 
@@ -615,6 +713,30 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
   }
   __syncthreads();
   if (prev == gridDim.x - 1) {  // the last CTA: convert the keys and re-zero the workspace
+    if (p.logprob != nullptr) {
+      // combine the per-CTA log-sum-exp partials: CTA b goes to thread b mod
+      // blockDim, then a fixed shuffle tree and a fixed pass over the warps,
+      // so the result does not depend on which CTA finished last
+      for (int m = 0; m < M; ++m) {
+        float cm = -INFINITY, cs = 0.f;
+        for (unsigned int b = threadIdx.x; b < gridDim.x; b += blockDim.x) {
+          float2 v;
+          asm volatile("ld.relaxed.gpu.global.v2.f32 {%0, %1}, [%2];"
+                       : "=f"(v.x), "=f"(v.y)
+                       : "l"(p.lse + (int64_t)b * 8 + m)
+                       : "memory");
+          lse_merge(cm, cs, v.x, v.y);
+        }
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const float om = __shfl_xor_sync(0xFFFFFFFFu, cm, o);
+          const float os = __shfl_xor_sync(0xFFFFFFFFu, cs, o);
+          lse_merge(cm, cs, om, os);
+        }
+        if (lane == 0) lred[warp * 8 + m] = make_float2(cm, cs);
+      }
+      __syncthreads();
+    }
     if (threadIdx.x < (unsigned)M) {
       unsigned long long key;
       asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(key) : "l"(p.keys + threadIdx.x) : "memory");
@@ -623,14 +745,7 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
           key == 0ull ? 0 : (int32_t)(0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFull));
       if (p.logprob != nullptr) {
         float cm = -INFINITY, cs = 0.f;
-        for (unsigned int b = 0; b < gridDim.x; ++b) {
-          float2 v;
-          asm volatile("ld.relaxed.gpu.global.v2.f32 {%0, %1}, [%2];"
-                       : "=f"(v.x), "=f"(v.y)
-                       : "l"(p.lse + (int64_t)b * 8 + threadIdx.x)
-                       : "memory");
-          lse_merge(cm, cs, v.x, v.y);
-        }
+        for (int w = 0; w < kWarps; ++w) lse_merge(cm, cs, lred[w * 8 + threadIdx.x].x, lred[w * 8 + threadIdx.x].y);
         // the winning logit back from its key (inverse of the order-preserving map)
         const uint32_t o = (uint32_t)(key >> 32);
         const float ymax = __uint_as_float((o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o);
@@ -643,6 +758,20 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
 }
 
 using KernelFn = void (*)(CUtensorMap, GemvParams);
+using PrepFn = void (*)(GemvParams, uint2*, unsigned int*);
+
+PrepFn prep_for(int m) {
+  switch (m) {
+    case 1: return act_prep_kernel<1>;
+    case 2: return act_prep_kernel<2>;
+    case 3: return act_prep_kernel<3>;
+    case 4: return act_prep_kernel<4>;
+    case 5: return act_prep_kernel<5>;
+    case 6: return act_prep_kernel<6>;
+    case 7: return act_prep_kernel<7>;
+    default: return act_prep_kernel<8>;
+  }
+}
 
 template <int WARPS>
 KernelFn kernel_for(int m) {
@@ -670,7 +799,7 @@ Layout layout_for(int warps, int m, int nchunks) {
   l.off_red = (uint32_t)off;
   off += (size_t)warps * 32 * 4 * sizeof(float);
   l.off_small = (uint32_t)off;
-  off += (16 + 16 * warps + 8 + 16) * sizeof(float);
+  off += (size_t)small_floats(warps) * sizeof(float);
   off = (off + 15) & ~(size_t)15;
   l.off_kred = (uint32_t)off;
   off += (size_t)warps * 8 * sizeof(unsigned long long) + (size_t)warps * 8 * sizeof(float2);
@@ -678,7 +807,7 @@ Layout layout_for(int warps, int m, int nchunks) {
   l.off_ring = (uint32_t)off;
   off += (size_t)warps * kRing * kStageBytes;
   l.off_bar = (uint32_t)off;
-  off += (size_t)warps * kRing * 8;
+  off += (size_t)warps * kRing * 8 + 8;  // ring barriers + the fragment-copy barrier
   l.bytes = off + 1024;
   return l;
 }
@@ -687,8 +816,8 @@ Layout layout_for(int warps, int m, int nchunks) {
 
 int launch_gemv(const w4a16_act_segment* seg, int nseg, int m, const nvfp4_weight* w, void* y,
                 int y_dtype, int64_t ldy, bool want_argmax, int32_t* argmax, void* workspace,
-                int32_t* dev_status, cudaStream_t stream, float* logprob, const int32_t* mask,
-                int64_t ld_mask) {
+                size_t workspace_bytes, int32_t* dev_status, cudaStream_t stream, float* logprob,
+                const int32_t* mask, int64_t ld_mask) {
   GemvParams p{};
   for (int s = 0; s < 2; ++s) {
     p.x[s] = s < nseg ? reinterpret_cast<const __nv_bfloat16*>(seg[s].x) : nullptr;
@@ -751,11 +880,12 @@ int launch_gemv(const w4a16_act_segment* seg, int nseg, int m, const nvfp4_weigh
 
   const int sms = nvfp4::sm_count();
   const int64_t slots = (int64_t)sms * occ;  // resident CTAs
-  // Split K (ks warps per tile) until the resident CTAs each get several tile
-  // groups to stream, keeping at least 4 chunks per warp; split factors are 1,
-  // 4, 8, 16 (at most 4 tile groups per CTA share its named barriers).
+  // Split K (ks warps per tile) only while there are fewer tile groups than
+  // resident CTAs (the split-K hand-off costs more than the load imbalance it
+  // removes beyond that), keeping at least 4 chunks per warp; split factors
+  // are 1, 4, 8, 16 (at most 4 tile groups per CTA share its named barriers).
   int ks = 1;
-  while (ks < warps && nvfp4::cdiv(p.ntiles, warps / ks) < 4 * slots &&
+  while (ks < warps && nvfp4::cdiv(p.ntiles, warps / ks) < slots &&
          p.nchunks / kItem / (2 * ks) >= 2)
     ks = ks == 1 ? 4 : 2 * ks;
   if (ks > 1 && warps / ks > 4) ks = warps / 4;
@@ -763,14 +893,35 @@ int launch_gemv(const w4a16_act_segment* seg, int nseg, int m, const nvfp4_weigh
   const int64_t ngroups = nvfp4::cdiv(p.ntiles, warps / ks);
   int64_t grid = ngroups < slots ? ngroups : slots;
   if (grid > W4A16_GEMV_MAX_CTAS) grid = W4A16_GEMV_MAX_CTAS;  // bound of the log-prob workspace
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  // With room in the workspace and more than one batch row, one small grid
+  // normalises the activations once (one CTA per batch row) and every GEMV
+  // CTA copies its result.  At m = 1 the per-CTA prologue is short and mostly
+  // hidden behind the first weight loads; the extra launch costs more.
+  const bool prep = m >= 2 && workspace != nullptr &&
+                    workspace_bytes >= W4A16_GEMV_WS_BYTES(m, w->k) && nvfp4::aligned16(workspace);
+  if (prep) {
+    char* ws = reinterpret_cast<char*>(workspace);
+    unsigned int* rowmax = reinterpret_cast<unsigned int*>(ws + W4A16_GEMV_PREP_OFFSET);
+    uint2* frag = reinterpret_cast<uint2*>(ws + W4A16_GEMV_PREP_OFFSET + 256);
+    p.frag_src = frag;
+    p.rowmax_src = rowmax;
+    cudaLaunchConfig_t pc = {};
+    pc.gridDim = dim3((unsigned)m);
+    pc.blockDim = dim3(512);
+    pc.dynamicSmemBytes = 0;
+    pc.stream = stream;
+    pc.attrs = attr;
+    pc.numAttrs = 1;
+    if (cudaLaunchKernelEx(&pc, prep_for(m), p, frag, rowmax) != cudaSuccess) return NVFP4_ERR_CUDA;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
   cfg.blockDim = dim3(warps * 32);
   cfg.dynamicSmemBytes = lay.bytes;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   if (cudaLaunchKernelEx(&cfg, fn, tmap, p) != cudaSuccess) return NVFP4_ERR_CUDA;

@@ -5,8 +5,9 @@
 Cases (seeded synthetic inputs of the draft head's workloads, built on the
 device): ``lm_head`` (32768 x 4096, RMSNorm + GEMV + argmax, M=1), ``propose``
 (151936 x 5120 GEMV + argmax, M=--m), ``fc`` (5120 x 10240, two RMSNorms +
-concat, BF16 out, M=--m), ``gemm`` (2048 x 17408 x 5120 prefill GEMM, FP16
-staging workspace as the benchmark times it),
+concat, BF16 out, M=--m), ``gemm`` (2048 x 17408 x 5120 prefill GEMM on BF16
+operands, as the benchmark times it; ``gemm_f16`` with the FP16 staging
+workspace),
 ``quantize`` (17408 x 5120).  Inputs are prepared first (their kernels run
 before the measured calls, so ``ncu -k regex:<kernel> -s <n>`` can skip them),
 then the call runs --iters times and the process exits 0.
@@ -27,7 +28,7 @@ def main():
     import workloads
     ap = argparse.ArgumentParser()
     ap.add_argument("--case", required=True,
-                    choices=["lm_head", "propose", "fc", "gemm", "quantize"])
+                    choices=["lm_head", "propose", "fc", "gemm", "gemm_f16", "quantize"])
     ap.add_argument("--m", type=int, default=1)
     ap.add_argument("--iters", type=int, default=3)
     args = ap.parse_args()
@@ -57,10 +58,12 @@ def main():
         torch.cuda.synchronize()
         for _ in range(args.iters):
             nd.w4a16_gemv([(e, ge, 1e-6), (h, gh, 1e-6)], wq, out_dtype=torch.bfloat16)
-    elif args.case == "gemm":
+    elif args.case in ("gemm", "gemm_f16"):
         c = workloads.prefill_gemm(device=dev)
         wq, _ = nd.nvfp4_quantize(c.w)
-        ws = torch.empty(nd.gemm_workspace_bytes(2048, 5120), dtype=torch.uint8, device=dev)
+        ws = None
+        if args.case == "gemm_f16":
+            ws = torch.empty(nd.gemm_workspace_bytes(2048, 5120), dtype=torch.uint8, device=dev)
         torch.cuda.synchronize()
         for _ in range(args.iters):
             nd.w4a16_gemm(c.a, wq, workspace=ws)

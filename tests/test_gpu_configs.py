@@ -204,8 +204,8 @@ def test_prefill_gemm_config_sampled(dev):
     wb = workloads.bits(case.w)
     g = check_gpu_quant(wq, amax, wb)
     ws = torch.empty(m.gemm_workspace_bytes(2048, 5120), dtype=torch.uint8, device=dev)
-    c = m.w4a16_gemm(case.a, wq, workspace=ws)   # the launch the benchmark times
-    c_bf16 = m.w4a16_gemm(case.a, wq)
+    c = m.w4a16_gemm(case.a, wq, workspace=ws)   # FP16 staging path
+    c_bf16 = m.w4a16_gemm(case.a, wq)            # the launch the benchmark times
     torch.cuda.synchronize()
     rng = np.random.default_rng(12)
     rows = np.concatenate([rng.integers(0, 2048, 8192), np.full(17408, 5), np.full(17408, 2047),

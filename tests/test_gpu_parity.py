@@ -201,6 +201,38 @@ def test_gemv_strided_activations(dev):
     assert np.all(np.isnan(o[:, 300:])), "wrote outside the output rows"
 
 
+@pytest.mark.parametrize("m_rows,n,k1,k2", [(2, 300, 1056, 0), (3, 1000, 512, 544), (8, 257, 2048, 1024)])
+def test_prepared_activations_match_in_kernel_prologue(dev, m_rows, n, k1, k2):
+    """The once-per-call activation grid (large workspace) and the per-CTA
+    prologue (small or no workspace) give bit-identical logits and argmax."""
+    m = nd()
+    g = torch.Generator().manual_seed(n + k1 + k2)
+    k = k1 + k2
+    w = (torch.randn((n, k), generator=g) * 0.02).to(torch.bfloat16)
+    wq, _ = m.nvfp4_quantize(w.to(dev))
+    segs = []
+    for ks in (k1, k2):
+        if ks == 0:
+            continue
+        x = (torch.randn((m_rows, ks + 16), generator=g) * 3).to(torch.bfloat16)[:, 8:8 + ks]
+        gamma = (1 + 0.05 * torch.randn(ks, generator=g)).to(torch.bfloat16)
+        segs.append((x.to(dev), gamma.to(dev), 1e-6))
+    big = torch.zeros(m.gemv_workspace_bytes(m_rows, k), dtype=torch.uint8, device=dev)
+    small = torch.zeros(m.ARGMAX_WS_BYTES, dtype=torch.uint8, device=dev)
+    lg_p, idx_p = m.w4a16_gemv_argmax(segs, wq, workspace=big)
+    lg_k, idx_k = m.w4a16_gemv_argmax(segs, wq, workspace=small)
+    y_p = m.w4a16_gemv(segs, wq, out_dtype=torch.bfloat16, workspace=big)
+    y_k = m.w4a16_gemv(segs, wq, out_dtype=torch.bfloat16, prepare=False)
+    torch.cuda.synchronize()
+    assert torch.equal(lg_p, lg_k) and torch.equal(idx_p, idx_k)
+    assert torch.equal(y_p.view(torch.int16), y_k.view(torch.int16))
+    a = oracle.rmsnorm_concat([(workloads.bits(x.cpu()), workloads.bits(gm.cpu()), e) for x, gm, e in segs],
+                              m_rows)
+    y, sabs = oracle.gemv(a, wq.packed.cpu().numpy(), wq.scales.cpu().numpy(),
+                          np.float32(wq.global_scale.item()))
+    check_logits(lg_p.cpu().numpy(), y, sabs)
+
+
 def test_argmax_ties_pick_lowest_index(dev):
     m = nd()
     case = workloads.propose_m8(n=700, k=256, m=2)
