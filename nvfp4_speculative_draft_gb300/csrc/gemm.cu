@@ -7,21 +7,23 @@
 // FP4 weight is dequantised exactly to BF16 and multiplied with BF16 MMAs
 // accumulating in FP32, one 128-row tile of A at a time.
 //
-// One CTA computes a 128 x 256 output tile (M = 128 activation rows, N = 256
-// weight rows) with tcgen05.mma (cta_group::1, kind::f16, BF16 x BF16 -> FP32),
-// the accumulator in tensor memory (256 TMEM columns).  K runs in steps of 64
-// through shared-memory rings (4 stages of A, 4 of B):
-//   warp 0      TMA producer: the 128 x 64 BF16 A tile by cp.async.bulk.tensor
-//               (128-byte swizzle; rows past m read as zero);
-//   warp 1      allocates TMEM, issues the 4 MMAs (K = 16 each) of a stage from
-//               one thread, commits each stage's completion to its "empty"
-//               barrier and the last one to the accumulator barrier;
-//   warps 2..9  dequantise the 256 x 64 weight tile (one row per thread: 32
-//               bytes of codes + 4 scale bytes, prefetched one step ahead) into
-//               the same 128-byte-swizzled K-major layout, fence the async proxy
-//               and arrive on the stage's "full" barrier; after the K loop they
-//               are the epilogue: tcgen05.ld of their TMEM lane quadrant, times
-//               g, round to BF16, store.
+// One persistent CTA per SM computes 256 x 256 output tiles (256 activation
+// rows, 256 weight rows) as two 128 x 256 tcgen05.mma tiles (cta_group::1,
+// kind::f16, BF16 x BF16 -> FP32) that share every dequantised weight tile,
+// their accumulators side by side in tensor memory (2 x 256 columns).  K runs
+// in steps of 64 through shared-memory rings (3 stages of A, 3 of B):
+//   warp 0       TMA producer: the two 128 x 64 BF16 A boxes of a step by
+//                cp.async.bulk.tensor (128-byte swizzle; rows past m read as 0);
+//   warp 1       allocates TMEM; one thread issues the 8 MMAs of a step (K = 16,
+//                two halves), commits each stage's completion to its "empty"
+//                barriers and a tile's last one to the accumulator barrier;
+//   warps 2..17  dequantise the 256 x 64 weight tile (two threads per row,
+//                32 K-elements each, four steps of loads in flight) into the
+//                same 128-byte-swizzled K-major layout, fence the async proxy
+//                and arrive on the stage's "full" barrier;
+//   warps 18..21 epilogue: tcgen05.ld of their TMEM lane quadrant for both
+//                halves, times g, round to BF16, store; then release TMEM to
+//                the next tile.
 // Dequantisation: E2M1 nibble pairs become BF16 bit patterns of value * 2^-126
 // (integer ops), then one packed BF16 multiply by the block scale * 2^118
 // (exact); the 2^8 left over is folded into g in the epilogue.
@@ -35,19 +37,30 @@
 
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 64;
-// Ring depths (A tiles by TMA, B tiles by the dequantising warps).  4 + 4 was
-// the fastest of the splits that fit (2+5, 3+5, 4+4, 5+4, 7+3 measured).
-constexpr int kStagesA = 4;
-constexpr int kStagesB = 4;
-constexpr int kABytes = BM * BK * 2;  // 16 KB
+constexpr int BM = 128, BN = 256, BK = 64;  // one MMA: 128 x 256, K steps of 64
+// An output tile is kMHalves MMA tiles high: both halves share each dequantised
+// B tile, so the dequantisation per FLOP halves with two.  Their accumulators
+// then fill TMEM (2 x 256 columns) and the epilogue no longer overlaps the
+// next tile's MMAs; with one half, the two accumulators double-buffer tiles.
+constexpr int kMHalves = 2;
+constexpr int BMT = BM * kMHalves;  // output tile rows
+constexpr bool kSingleBuf = 2 * kMHalves * BN > 512;  // TMEM holds one tile's accumulators only
+// Ring depths (A tiles by TMA, B tiles by the dequantising warps); measured
+// best: 3 + 3 with two halves (2+4, 4+2, 2+3 slower), 4 + 4 with one.  Also
+// measured: 128-column tiles with four halves (N = 128 MMAs) are slower.
+constexpr int kStagesA = kMHalves == 2 ? 3 : 4;
+constexpr int kStagesB = kMHalves == 2 ? 3 : 4;
+constexpr int kAHalfBytes = BM * BK * 2;          // 16 KB
+constexpr int kABytes = kMHalves * kAHalfBytes;
 constexpr int kBBytes = BN * BK * 2;  // 32 KB
 constexpr int kRingABytes = kStagesA * kABytes;
 constexpr int kRingBytes = kRingABytes + kStagesB * kBBytes;
-constexpr int kDequantWarps = 16;  // two threads per weight row, 32 K-elements each
+constexpr int kDequantWarps = BN / 16;  // two threads per weight row, 32 K-elements each
 constexpr int kEpilogueWarps = 4;
 constexpr int kThreads = (2 + kDequantWarps + kEpilogueWarps) * 32;
-constexpr int kTmemCols = 2 * BN;  // two accumulators: epilogue of one tile overlaps the next
+// TMEM columns: two tiles' accumulators (the epilogue of one overlaps the
+// next tile's MMAs) or one tile's kMHalves accumulators
+constexpr int kTmemCols = kSingleBuf ? kMHalves * BN : 2 * kMHalves * BN;
 constexpr int kPrefetch = 4;       // k steps of weight rows in flight per dequant thread
 constexpr size_t kSmemBytes = 1024 /*alignment slack*/ + (size_t)kRingBytes + 256;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
@@ -242,7 +255,7 @@ struct GemmParams {
 // Tile t of the persistent schedule: consecutive t share one 256-row weight
 // slice (n tile), so the CTAs working on it at the same time find it in L2.
 __device__ __forceinline__ void tile_coords(const GemmParams& p, int t, int64_t& m0, int64_t& n0) {
-  m0 = (int64_t)(t % p.mtiles) * BM;
+  m0 = (int64_t)(t % p.mtiles) * BMT;
   n0 = (int64_t)(t / p.mtiles) * BN;
 }
 
@@ -319,7 +332,10 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
         tile_coords(p, (int)blockIdx.x + (g / nk) * (int)gridDim.x, m0, n0);
         if (r > 0 && !mbar_wait(empty_a(s), (r - 1) & 1, abort, p.dev_status)) break;
         mbar_arrive_expect_tx(full_a(s), kABytes);
-        tma_load_2d(a_tile(s), &tmap_a, kb * BK, (int)m0, full_a(s));
+#pragma unroll
+        for (int h = 0; h < kMHalves; ++h)
+          tma_load_2d(a_tile(s) + (uint32_t)(h * kAHalfBytes), &tmap_a, kb * BK, (int)m0 + h * BM,
+                      full_a(s));
       }
     }
   } else if (warp == 1) {
@@ -327,10 +343,12 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
     if (lane == 0) {
       bool ok = true;
       for (int it = 0; it < my_tiles && ok; ++it) {
-        const int ab = it & 1;
-        if (it >= 2 && !mbar_wait(tmem_empty(ab), ((it >> 1) - 1) & 1, abort, p.dev_status)) break;
+        // accumulator buffer: the tile's halves fill TMEM, or tiles alternate
+        const int ab = kSingleBuf ? 0 : (it & 1);
+        const int nb = kSingleBuf ? 1 : 2;  // tiles per buffer reuse cycle
+        if (it >= nb && !mbar_wait(tmem_empty(ab), ((it / nb) - 1) & 1, abort, p.dev_status)) break;
         tc_fence_after();
-        const uint32_t d = tmem + (uint32_t)(ab * BN);
+        const uint32_t d = tmem + (uint32_t)(ab * kMHalves * BN);
         for (int kb = 0; kb < nk; ++kb) {
           const int g = it * nk + kb;
           const int sa = g % kStagesA, ra = g / kStagesA;
@@ -342,8 +360,12 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
           const uint64_t ad = smem_desc(a_tile(sa));
           const uint64_t bd = smem_desc(base + b_tile(sb));
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk)  // advance 32 bytes (16 BF16) along K
-            mma_f16kind(d, ad + 2 * kk, bd + 2 * kk, kIdesc, (kb > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < BK / 16; ++kk) {  // advance 32 bytes (16 BF16) along K
+#pragma unroll
+            for (int h = 0; h < kMHalves; ++h)
+              mma_f16kind(d + (uint32_t)(h * BN), ad + (uint64_t)(h * (kAHalfBytes >> 4)) + 2 * kk,
+                          bd + 2 * kk, kIdesc, (kb > 0 || kk > 0) ? 1u : 0u);
+          }
           mma_commit(empty_a(sa));  // both commits track the same MMAs
           mma_commit(empty_b(sb));
         }
@@ -430,20 +452,21 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
     // BF16 path: g * 2^8 (the dequant fold); FP16 path: g, and 2^-e per row
     const float gs = F16 ? __ldg(p.gscale) : __ldg(p.gscale) * 256.0f;
     for (int it = 0; it < my_tiles; ++it) {
-      const int ab = it & 1;
+      const int ab = kSingleBuf ? 0 : (it & 1);
+      const int nb = kSingleBuf ? 1 : 2;
       __syncwarp();
-      if (!mbar_wait(tmem_full(ab), (it >> 1) & 1, abort, p.dev_status)) break;
+      if (!mbar_wait(tmem_full(ab), (it / nb) & 1, abort, p.dev_status)) break;
       __syncwarp();
       tc_fence_after();
       int64_t m0, n0;
       tile_coords(p, (int)blockIdx.x + it * (int)gridDim.x, m0, n0);
-      const int64_t row = m0 + 32 * q + lane;
-      const float rs = (F16 && row < p.m) ? __ldg(p.row_inv + row) : 1.0f;
 #pragma unroll 1
-      for (int j = 0; j < BN / 32; ++j) {
-        const int col = 32 * j;
+      for (int hj = 0; hj < kMHalves * (BN / 32); ++hj) {
+        const int h = hj / (BN / 32), col = 32 * (hj % (BN / 32));
+        const int64_t row = m0 + h * BM + 32 * q + lane;
+        const float rs = (F16 && row < p.m) ? __ldg(p.row_inv + row) : 1.0f;
         uint32_t v[32];
-        tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(ab * BN + col), v);
+        tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)((ab * kMHalves + h) * BN + col), v);
         if (row < p.m && n0 + col < p.n) {
           uint32_t packed16[16];
 #pragma unroll
@@ -557,7 +580,7 @@ int launch_gemm(const void* a, int64_t m, int64_t lda, const nvfp4_weight* w, vo
   p.n = w->n;
   p.k = w->k;
   p.ldc = ldc;
-  p.mtiles = (int)nvfp4::cdiv(m, BM);
+  p.mtiles = (int)nvfp4::cdiv(m, BMT);
   p.ntiles = (int)nvfp4::cdiv(w->n, BN);
   p.row_inv = row_inv;
   p.dev_status = dev_status;
