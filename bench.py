@@ -306,7 +306,35 @@ def bench_details(dev, stream, hbm, bf16):
             prop[f"M{m}_mask_logprob"] = {"us": ms_ex * 1e3, "GBps": b / ms_ex / 1e6,
                                           "frac_of_measured_hbm": b / ms_ex / 1e6 / hbm}
     out["propose_151936x5120"] = prop
-    del wq
+    # chained propose step (M = 1): fc 5120 x 10240 over [norm(embed[token]),
+    # norm(hidden)] -> BF16 hidden -> LM head 151936 x 5120 over norm_f(hidden)
+    # -> token, which the next step's fc gathers on the device
+    fcase = workloads.fc_combiner(device=dev)
+    fcw, _ = nd.nvfp4_quantize(fcase.w)
+    del fcase.w
+    (e0, ge), (h0, gh) = fcase.segments
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(4242)
+    emb = (torch.randn((151936, 5120), generator=gen, device=dev)).to(torch.bfloat16)
+    gf = (1 + 0.05 * torch.randn(5120, generator=gen, device=dev)).to(torch.bfloat16)
+    tok = torch.zeros((1,), dtype=torch.int32, device=dev)
+    hbuf = [h0[:1].contiguous(), torch.empty((1, 5120), dtype=torch.bfloat16, device=dev)]
+    steps = 10
+
+    def chain():
+        for i in range(steps):  # the hidden state ping-pongs between two buffers
+            hid, ybuf = hbuf[i % 2], hbuf[(i + 1) % 2]
+            nd.w4a16_gemv([(emb, ge, 1e-6, tok), (hid, gh, 1e-6)], fcw, out=ybuf, stream=stream)
+            nd.w4a16_gemv_argmax([(ybuf, gf, 1e-6)], wq, logits=False, out_argmax=tok, stream=stream)
+    ms = time_graph(chain, stream, 5) / steps
+    b = gemv_bytes(5120, 10240, 1, nseg_gamma_k=10240, out_bytes_per=2, argmax=False) \
+        + gemv_bytes(151936, 5120, 1, nseg_gamma_k=5120, out_bytes_per=0)
+    out["chained_propose_step"] = {"us_per_step": ms * 1e3, "GBps": b / ms / 1e6,
+                                   "frac_of_measured_hbm": b / ms / 1e6 / hbm,
+                                   "note": "fc (embedding gathered by the previous token on "
+                                           "the device) + LM head + argmax, M=1, graph of "
+                                           f"{steps} chained steps"}
+    del wq, fcw, emb, hbuf
     # fc combiner 5120 x 10240 (29.5 MB: rotate copies)
     base = workloads.fc_combiner(device=dev)
     wbytes = 5120 * 10240 // 2 + 5120 * 10240 // 16

@@ -50,6 +50,7 @@ extern "C" {
 #define NVFP4_ERR_TIMEOUT 6    /* device: a bounded wait gave up             */
 #define NVFP4_ERR_NONFINITE 7  /* device: Inf/NaN in the quantiser's input   */
 #define NVFP4_ERR_DTYPE 8      /* unknown output dtype                       */
+#define NVFP4_ERR_INDEX 9      /* device: a gather index out of range; row 0 */
 
 /* Output element types. */
 #define NVFP4_DTYPE_F32 0
@@ -105,6 +106,15 @@ typedef struct w4a16_act_segment {
     int64_t ld;         /* row stride in elements, multiple of 8, >= k_seg        */
     const void *gamma;  /* BF16 [k_seg], 16-B aligned, or NULL for no norm        */
     float eps;
+    /* Optional gather (embed_from_argmax of "metrale_model_layers/layers/
+     * mtp_head.rs", fused into the activation load): with row_index != NULL,
+     * x is a table of index_rows rows and row r of the segment is table row
+     * row_index[r] -- e.g. the embedding of the token the previous
+     * w4a16_gemv_argmax call wrote to its device argmax buffer, read after
+     * that call completes (stream order), with no host round trip.  An index
+     * outside [0, index_rows) reads row 0 and records NVFP4_ERR_INDEX. */
+    const int32_t *row_index;  /* device int32 [m], 4-B aligned, or NULL      */
+    int64_t index_rows;        /* rows of the table when row_index != NULL   */
 } w4a16_act_segment;
 
 /* Execution context. */

@@ -25,8 +25,9 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "_build", "libnvfp4draft.so")
 
 NVFP4_OK = 0
+NVFP4_ERR_INDEX = 9
 STATUS_NAMES = {0: "OK", 1: "ERR_NULL", 2: "ERR_SHAPE", 3: "ERR_ALIGN", 4: "ERR_WORKSPACE",
-                5: "ERR_CUDA", 6: "ERR_TIMEOUT", 7: "ERR_NONFINITE", 8: "ERR_DTYPE"}
+                5: "ERR_CUDA", 6: "ERR_TIMEOUT", 7: "ERR_NONFINITE", 8: "ERR_DTYPE", 9: "ERR_INDEX"}
 DTYPE_F32 = 0
 DTYPE_BF16 = 1
 GEMV_MAX_M = 8
@@ -58,7 +59,8 @@ class _Weight(ctypes.Structure):
 
 class _Segment(ctypes.Structure):
     _fields_ = [("x", ctypes.c_void_p), ("k_seg", ctypes.c_int64), ("ld", ctypes.c_int64),
-                ("gamma", ctypes.c_void_p), ("eps", ctypes.c_float)]
+                ("gamma", ctypes.c_void_p), ("eps", ctypes.c_float),
+                ("row_index", ctypes.c_void_p), ("index_rows", ctypes.c_int64)]
 
 
 class _Exec(ctypes.Structure):
@@ -162,22 +164,33 @@ def nvfp4_quantize(w: torch.Tensor, out: Optional[Nvfp4Weight] = None, absmax: O
     return out, absmax
 
 
-def _segments(segments: Sequence) -> tuple:
-    """segments: [(x [m, k_seg] bf16, gamma [k_seg] bf16 or None, eps), ...]"""
+def _segments(segments: Sequence, m: Optional[int] = None) -> tuple:
+    """segments: [(x, gamma or None, eps[, row_index]), ...].
+
+    x is BF16 [m, k_seg] with unit column stride; or, with ``row_index`` (a
+    device int32 tensor of m indices, e.g. the argmax output of the previous
+    call), a BF16 table [rows, k_seg] whose rows row_index[r] are gathered."""
     arr = (_Segment * len(segments))()
-    m = None
     for i, s in enumerate(segments):
         s = tuple(s)
         x = s[0]
         gamma = s[1] if len(s) > 1 else None
         eps = s[2] if len(s) > 2 else 1e-6
+        ridx = s[3] if len(s) > 3 else None
         assert x.dtype == torch.bfloat16 and x.dim() == 2 and x.stride(1) == 1 and x.is_cuda
         if gamma is not None:
             assert gamma.dtype == torch.bfloat16 and gamma.is_contiguous()
+        if ridx is not None:
+            assert ridx.dtype == torch.int32 and ridx.dim() == 1 and ridx.is_contiguous()
+            rows = ridx.shape[0]
+        else:
+            rows = x.shape[0]
         arr[i] = _Segment(x.data_ptr(), x.shape[1], x.stride(0),
-                          gamma.data_ptr() if gamma is not None else None, float(eps))
-        m = x.shape[0] if m is None else m
-        assert x.shape[0] == m
+                          gamma.data_ptr() if gamma is not None else None, float(eps),
+                          ridx.data_ptr() if ridx is not None else None,
+                          x.shape[0] if ridx is not None else 0)
+        m = rows if m is None else m
+        assert rows == m, "every segment needs the same number of rows"
     return arr, m
 
 

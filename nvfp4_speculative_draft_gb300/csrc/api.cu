@@ -85,6 +85,10 @@ int check_segments(const w4a16_act_segment* seg, int nseg, int m, int64_t k) {
     if (seg[s].ld % 8 != 0 || !aligned16(seg[s].x)) return NVFP4_ERR_ALIGN;
     if (seg[s].gamma != nullptr && !aligned16(seg[s].gamma)) return NVFP4_ERR_ALIGN;
     if (seg[s].gamma != nullptr && !(seg[s].eps >= 0.0f)) return NVFP4_ERR_SHAPE;
+    if (seg[s].row_index != nullptr) {
+      if (reinterpret_cast<uintptr_t>(seg[s].row_index) & 3u) return NVFP4_ERR_ALIGN;
+      if (seg[s].index_rows < 1) return NVFP4_ERR_SHAPE;
+    }
     total += seg[s].k_seg;
   }
   if (total != k) return NVFP4_ERR_SHAPE;

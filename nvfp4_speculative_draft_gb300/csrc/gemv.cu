@@ -55,6 +55,8 @@ constexpr int kL2Prefetch = 4;    // items per warp pulled into L2 while the pre
 
 struct GemvParams {
   const __nv_bfloat16* x[2];
+  const int32_t* ridx[2];  // gather indices per segment, or null
+  int64_t tab_rows[2];     // rows of a gathered segment's table
   const __nv_bfloat16* gamma[2];
   int64_t kseg[2];
   int64_t ld[2];
@@ -239,6 +241,20 @@ __device__ __forceinline__ float row_scale_pow2(unsigned int maxbits, bool inver
 // uint2 at bfrag[q * 4M + L].  For the 8 activations at
 // kk = 128 c + 32 t + 8 w (+0..7):  MMA 8c+2w gets {a0,a4},{a1,a5};
 // MMA 8c+2w+1 gets {a2,a6},{a3,a7}.  Positions past k are zero.
+// Row r of segment s: row r of x, or, for a gathered segment, table row
+// ridx[r] (out-of-range indices read row 0 and are reported).
+__device__ __forceinline__ const __nv_bfloat16* seg_row(const GemvParams& p, int s, int r) {
+  int64_t row = r;
+  if (p.ridx[s] != nullptr) {
+    row = __ldg(p.ridx[s] + r);
+    if (row < 0 || row >= p.tab_rows[s]) {
+      nvfp4::report(p.dev_status, NVFP4_ERR_INDEX);
+      row = 0;
+    }
+  }
+  return p.x[s] + row * p.ld[s];
+}
+
 // Shared "small" area (floats): [0,16) inverse RMS per (row, segment);
 // [16,24) per-row scale exponent carrier (BF16 magnitude bits, see
 // row_scale_pow2); [24,26) max |gamma| per segment; [32,48) max |x| per
@@ -277,7 +293,7 @@ __device__ __noinline__ void build_fragments(const GemvParams& p, uint2* bfrag, 
       const int s = job < JR ? job % p.nseg : job - JR;
       const bool is_gamma = job >= JR;
       const __nv_bfloat16* src =
-          is_gamma ? p.gamma[s] : p.x[s] + (int64_t)(r0 + job / p.nseg) * p.ld[s];
+          is_gamma ? p.gamma[s] : seg_row(p, s, r0 + job / p.nseg);
       const bool want_ss = !is_gamma && p.gamma[s] != nullptr;
       float ss = 0.0f;
       uint32_t mx = 0u;
@@ -354,7 +370,7 @@ __device__ __noinline__ void build_fragments(const GemvParams& p, uint2* bfrag, 
       const int s = (p.nseg == 2 && kk >= p.kseg[0]) ? 1 : 0;
       const int ko = kk - (s ? (int)p.kseg[0] : 0);
       if (kk < p.k && NVFP4_GUARD(ko >= 0 && ko + 8 <= p.kseg[s], 2, p.dev_status)) {
-        const uint4 v = *reinterpret_cast<const uint4*>(p.x[s] + (int64_t)r * p.ld[s] + ko);
+        const uint4 v = *reinterpret_cast<const uint4*>(seg_row(p, s, r) + ko);
         a[0] = v.x; a[1] = v.y; a[2] = v.z; a[3] = v.w;
         if (p.gamma[s] != nullptr) {
           const uint4 gv = *reinterpret_cast<const uint4*>(p.gamma[s] + ko);
@@ -821,6 +837,8 @@ int launch_gemv(const w4a16_act_segment* seg, int nseg, int m, const nvfp4_weigh
   GemvParams p{};
   for (int s = 0; s < 2; ++s) {
     p.x[s] = s < nseg ? reinterpret_cast<const __nv_bfloat16*>(seg[s].x) : nullptr;
+    p.ridx[s] = s < nseg ? seg[s].row_index : nullptr;
+    p.tab_rows[s] = s < nseg ? seg[s].index_rows : 0;
     p.gamma[s] = s < nseg ? reinterpret_cast<const __nv_bfloat16*>(seg[s].gamma) : nullptr;
     p.kseg[s] = s < nseg ? seg[s].k_seg : 0;
     p.ld[s] = s < nseg ? seg[s].ld : 0;

@@ -128,6 +128,17 @@ def test_gemv_argmax_ex_argument_checks(L):
              ctypes.byref(ok)) == 2
 
 
+def test_gather_segment_argument_checks(L):
+    import nvfp4_speculative_draft_gb300 as nd
+    w = _weight(nd)
+    ex = nd._Exec(None, None, 0, None)
+    f = L.w4a16_gemv
+    bad_align = (nd._Segment * 1)(nd._Segment(0x4000, 512, 512, None, 1e-6, 0x7002, 100))
+    assert f(bad_align, 1, 1, ctypes.byref(w), 0x6000, 0, 256, ctypes.byref(ex)) == 3
+    no_rows = (nd._Segment * 1)(nd._Segment(0x4000, 512, 512, None, 1e-6, 0x7000, 0))
+    assert f(no_rows, 1, 1, ctypes.byref(w), 0x6000, 0, 256, ctypes.byref(ex)) == 2
+
+
 def test_gemm_argument_checks(L):
     import nvfp4_speculative_draft_gb300 as nd
     ex = nd._Exec(None, None, 0, None)

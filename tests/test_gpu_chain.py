@@ -1,0 +1,111 @@
+"""GPU parity of the chained propose step: the draft token the LM-head call
+writes to its device argmax buffer selects, with no host round trip, the
+embedding row that the next fc call normalises and concatenates with the
+hidden state (embed_from_argmax fused into the fc GEMV's activation load).
+
+Bars: a gathered segment gives bit-identical results to the same rows passed
+explicitly; each chained step's fc output is within 1e-3 * S + 1e-6 (+ one
+BF16 ulp) of the oracle computed from the GPU's previous outputs, and its
+token equals the oracle's argmax whenever the oracle's top-2 gap exceeds the
+tolerances (else it is inside the near-max set).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+TOL_REL, TOL_ABS = 1e-3, 1e-6
+
+
+def nd():
+    import nvfp4_speculative_draft_gb300 as m
+    return m
+
+
+def rand_bf16(shape, std, seed, dev, mean=0.0):
+    g = torch.Generator().manual_seed(seed)
+    return (torch.randn(shape, generator=g) * std + mean).to(torch.bfloat16).to(dev)
+
+
+@pytest.mark.parametrize("m_rows", [1, 3, 8])
+def test_gathered_segment_matches_explicit_rows(dev, m_rows):
+    m = nd()
+    V, H, N = 300, 512, 700
+    table = rand_bf16((V, H), 1.0, 1, dev)
+    h = rand_bf16((m_rows, H), 1.0, 2, dev)
+    ge, gh = rand_bf16((H,), 0.05, 3, dev, 1.0), rand_bf16((H,), 0.05, 4, dev, 1.0)
+    w = rand_bf16((N, 2 * H), 0.02, 5, dev)
+    wq, _ = m.nvfp4_quantize(w)
+    idx = torch.tensor([5, 299, 0, 17, 150, 5, 298, 1][:m_rows], dtype=torch.int32, device=dev)
+    e = table[idx.long()].contiguous()
+    for prepare in (False, True):
+        y_g = m.w4a16_gemv([(table, ge, 1e-6, idx), (h, gh, 1e-6)], wq, out_dtype=torch.bfloat16,
+                           prepare=prepare)
+        y_e = m.w4a16_gemv([(e, ge, 1e-6), (h, gh, 1e-6)], wq, out_dtype=torch.bfloat16,
+                           prepare=prepare)
+        torch.cuda.synchronize()
+        assert torch.equal(y_g.view(torch.int16), y_e.view(torch.int16))
+
+
+def test_gather_index_out_of_range_reads_row_zero_and_reports(dev):
+    m = nd()
+    V, H, N = 64, 256, 128
+    table = rand_bf16((V, H), 1.0, 6, dev)
+    w = rand_bf16((N, H), 0.02, 7, dev)
+    wq, _ = m.nvfp4_quantize(w)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    idx = torch.tensor([-1, 64, 3], dtype=torch.int32, device=dev)
+    y = m.w4a16_gemv([(table, None, 1e-6, idx)], wq, dev_status=status)
+    ref = m.w4a16_gemv([(table[[0, 0, 3]].contiguous(), None)], wq)
+    torch.cuda.synchronize()
+    assert status.item() == m.NVFP4_ERR_INDEX
+    assert torch.equal(y, ref)
+
+
+def test_chained_propose_steps_match_oracle(dev):
+    """Four draft steps: fc over [norm(embed[token]), norm(hidden)] -> BF16
+    hidden; LM head over norm_f(hidden) -> logits + token; the token feeds the
+    next step's gather on the device."""
+    m = nd()
+    V, H = 2048, 256
+    emb = rand_bf16((V, H), 1.0, 10, dev)
+    ge, gh, gf = (rand_bf16((H,), 0.05, s, dev, 1.0) for s in (11, 12, 13))
+    w_fc = rand_bf16((H, 2 * H), 0.015, 14, dev)
+    w_lm = rand_bf16((V, H), 0.02, 15, dev)
+    fc, _ = m.nvfp4_quantize(w_fc)
+    lm, _ = m.nvfp4_quantize(w_lm)
+    tok = torch.tensor([7], dtype=torch.int32, device=dev)
+    hid = rand_bf16((1, H), 1.0, 16, dev)
+    steps = []
+    for _ in range(4):
+        y = m.w4a16_gemv([(emb, ge, 1e-6, tok), (hid, gh, 1e-6)], fc, out_dtype=torch.bfloat16)
+        logits, nxt = m.w4a16_gemv_argmax([(y, gf, 1e-6)], lm)
+        steps.append((tok.clone(), hid.clone(), y.clone(), logits.clone(), nxt.clone()))
+        tok, hid = nxt, y
+    torch.cuda.synchronize()
+    b = workloads.bits
+    fcp, fcs, fcg = fc.packed.cpu().numpy(), fc.scales.cpu().numpy(), np.float32(fc.global_scale.item())
+    lmp, lms, lmg = lm.packed.cpu().numpy(), lm.scales.cpu().numpy(), np.float32(lm.global_scale.item())
+    for t, h, y, logits, nxt in steps:
+        e = emb[t.long()].cpu()
+        a = oracle.rmsnorm_concat([(b(e), b(ge.cpu()), 1e-6), (b(h.cpu()), b(gh.cpu()), 1e-6)], 1)
+        yx, ys = oracle.gemv(a, fcp, fcs, fcg)
+        got = y.float().cpu().numpy().astype(np.float64)
+        assert np.all(np.abs(got - yx) <= TOL_REL * ys + TOL_ABS + np.abs(yx) * 2.0 ** -8)
+        a2 = oracle.rmsnorm_concat([(b(y.cpu()), b(gf.cpu()), 1e-6)], 1)
+        lx, ls = oracle.gemv(a2, lmp, lms, lmg)
+        lg = logits.cpu().numpy().astype(np.float64)
+        tol = TOL_REL * ls + TOL_ABS
+        assert np.all(np.abs(lg - lx) <= tol)
+        i = int(nxt.item())
+        j = oracle.argmax(lx[0])
+        order = np.argsort(-lx[0], kind="stable")
+        second = order[1] if order[0] == j else order[0]
+        if lx[0, j] - lx[0, second] > tol[0, j] + tol[0, second]:
+            assert i == j
+        else:
+            assert lx[0, i] >= lx[0, j] - tol[0, i] - tol[0, j]
