@@ -79,6 +79,13 @@ def lib():
         L.oracle_argmax_masked.restype = _i64
         L.oracle_top1_logprob.argtypes = [_f64p, _i64, _i32p, _i64, _i64]
         L.oracle_top1_logprob.restype = ctypes.c_double
+        L.oracle_fp8_value.argtypes = [ctypes.c_int]
+        L.oracle_fp8_value.restype = ctypes.c_double
+        L.oracle_fp8_quantize_rows.argtypes = [_u16p, _i64, _i64, _i64, _u8p, _f32p]
+        L.oracle_fp8_quantize_rows.restype = ctypes.c_int
+        L.oracle_fp8_gemv_rows.argtypes = [_u16p, _i64, _i64, _u8p, _f32p, _i64, _i64, _i64,
+                                           _f64p, _f64p]
+        L.oracle_fp8_gemv_rows.restype = None
         _LIB = L
     return _LIB
 
@@ -272,3 +279,40 @@ def top1_logprob(y, idx, mask=None) -> float:
     return float(lib().oracle_top1_logprob(_ptr(y, _f64p), y.size,
                                            _ptr(mask, ctypes.POINTER(ctypes.c_int32)), mask.size,
                                            int(idx)))
+
+
+# ------------------------------------------------------------ FP8 weights
+
+def fp8_value(byte: int) -> float:
+    return lib().oracle_fp8_value(int(byte))
+
+
+def fp8_quantize(w_bits, rows=None):
+    """Per-row FP8 E4M3 quantisation of BF16 bits w[n, k] (all rows or the
+    given ones) -> (codes [r, k] u8, row scales [r] f32)."""
+    w = _c(w_bits, np.uint16)
+    n, k = w.shape
+    rows = np.arange(n) if rows is None else np.asarray(rows, dtype=np.int64)
+    codes = np.empty((len(rows), k), dtype=np.uint8)
+    scales = np.empty(len(rows), dtype=np.float32)
+    for j, r in enumerate(rows):
+        rc = lib().oracle_fp8_quantize_rows(_ptr(w, _u16p), k, int(r), 1, _ptr(codes[j], _u8p),
+                                            _ptr(scales[j:j + 1], _f32p))
+        if rc:
+            raise OracleError(f"oracle_fp8_quantize_rows rc={rc}")
+    return codes, scales
+
+
+def fp8_gemv(a_bits, codes, scales, n0=0, nn=None):
+    """Exact y[m, nn] and sabs[m, nn] for activation bits a[m, k]."""
+    a = _c(a_bits, np.uint16)
+    m, k = a.shape
+    codes = _c(codes, np.uint8)
+    scales = _c(scales, np.float32)
+    if nn is None:
+        nn = codes.shape[0] - n0
+    y = np.empty((m, nn), dtype=np.float64)
+    s = np.empty((m, nn), dtype=np.float64)
+    lib().oracle_fp8_gemv_rows(_ptr(a, _u16p), m, k, _ptr(codes, _u8p), _ptr(scales, _f32p), k,
+                               n0, nn, _ptr(y, _f64p), _ptr(s, _f64p))
+    return y, s

@@ -29,7 +29,7 @@
  * pages; it is taken from the project's problem statement and the public
  * OCP microscaling / NVFP4 format description.
  *
- * Readings taken where the pages are silent (each also listed in the design doc):
+ * Readings taken where the pages are silent:
  *   - quantiser arithmetic is this fixed sequence of binary32 operations:
  *       g   = fl32(amax / 2688)
  *       t_b = fl32(amax_b / fl32(6 * g));   s_b = E4M3_RNE_SATFINITE(t_b)
@@ -414,4 +414,71 @@ double oracle_top1_logprob(const double *y, int64_t n, const int32_t *mask, int6
         s += exp(y[i] - mx);
     }
     return y[idx] - (mx + log(s));
+}
+
+/* ------------------------------------------------------------ FP8 weights
+ * The pages' second projection precision: MtpHead::new
+ * ("spark_model/layers/mtp_head/new.rs") resolves gemv_fp8w's
+ * quantize_bf16_to_fp8 next to the NVFP4 pair, and the MtpQuantization::Fp8
+ * arm resolves dense_gemv_fp8w; neither formula is printed.  Reading (one
+ * kernel, so no separate global-absmax pass): E4M3 codes with one binary32
+ * scale per output row,
+ *     s_n = fl32(amax_n / 448),   c = E4M3_RNE_SATFINITE(fl32(x / s_n)),
+ * the sign bit of c the sign of x, every code +0 when s_n == 0; the GEMV is
+ *     y[m, n] = s_n * sum_i a[m, i] * e4m3(c[n, i]).
+ * Layout: codes [N, K] row-major, scales [N].
+ */
+double oracle_fp8_value(int byte)
+{
+    const double v = oracle_e4m3_value(byte & 0x7F);
+    return (byte & 0x80) ? -v : v;
+}
+
+int oracle_fp8_quantize_rows(const uint16_t *w, int64_t k, int64_t row0, int64_t nrows,
+                             uint8_t *codes, float *row_scale)
+{
+    for (int64_t r = 0; r < nrows; ++r) {
+        const uint16_t *x = w + (row0 + r) * k;
+        float amax = 0.0f;
+        for (int64_t i = 0; i < k; ++i) {
+            const float v = oracle_bf16_to_float(x[i]);
+            if (!isfinite(v))
+                return 1;
+            if (fabsf(v) > amax)
+                amax = fabsf(v);
+        }
+        const float s = amax / 448.0f; /* binary32 division */
+        row_scale[r] = s;
+        for (int64_t i = 0; i < k; ++i) {
+            const float v = oracle_bf16_to_float(x[i]);
+            if (s == 0.0f) {
+                codes[r * k + i] = 0;
+                continue;
+            }
+            const float q = v / s; /* binary32 division */
+            const int mag = oracle_e4m3_encode(fabsf(q));
+            codes[r * k + i] = (uint8_t)(mag | (signbit(v) ? 0x80 : 0));
+        }
+    }
+    return 0;
+}
+
+void oracle_fp8_gemv_rows(const uint16_t *a, int64_t m, int64_t lda, const uint8_t *codes,
+                          const float *row_scale, int64_t k, int64_t n0, int64_t nn,
+                          double *y, double *sabs)
+{
+    for (int64_t r = 0; r < m; ++r) {
+        for (int64_t j = 0; j < nn; ++j) {
+            double acc = 0.0, aacc = 0.0;
+            const double s = (double)row_scale[n0 + j];
+            for (int64_t i = 0; i < k; ++i) {
+                double p = (double)oracle_bf16_to_float(a[r * lda + i]) *
+                           (oracle_fp8_value(codes[(n0 + j) * k + i]) * s);
+                acc += p;
+                aacc += fabs(p);
+            }
+            y[r * nn + j] = acc;
+            sabs[r * nn + j] = aacc;
+        }
+    }
 }

@@ -396,3 +396,74 @@ def test_top1_logprob_against_scipy_logsumexp():
     assert oracle.top1_logprob(np.array([3.0, 50.0]), 0, _bits_to_mask([True, False])) == 0.0
     # uniform logits: log(1/n)
     assert abs(oracle.top1_logprob(np.zeros(64), 5) - np.log(1 / 64)) < 1e-15
+
+
+# ------------------------------------------------------------ FP8 weights
+
+def _fp8_decode(codes, scales):
+    """Independent dequantisation: torch's E4M3 decode times the row scale."""
+    vals = torch.from_numpy(np.ascontiguousarray(codes)).view(torch.float8_e4m3fn).to(torch.float64)
+    return vals.numpy() * scales.astype(np.float64)[:, None]
+
+
+def test_fp8_value_matches_torch_all_bytes():
+    allb = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    for b in range(256):
+        if (b & 0x7F) == 0x7F:
+            continue  # NaN encodings, never produced
+        assert oracle.fp8_value(b) == allb[b], b
+
+
+def test_fp8_quantize_lossless_round_trip_of_representable_rows():
+    """Rows s * v with s a power of two, v on the E4M3 grid and one |v| = 448:
+    the row scale comes out as s exactly and every code reproduces v."""
+    rng = np.random.default_rng(31)
+    grid = torch.arange(0, 127, dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    for s_exp in (-14, -9, -3, 0):
+        v = rng.choice(grid, size=(3, 64)) * rng.choice([-1.0, 1.0], size=(3, 64))
+        v[:, 5] = 448.0
+        s = 2.0 ** s_exp
+        x = torch.tensor(v * s, dtype=torch.float64).to(torch.bfloat16)
+        assert np.array_equal(x.double().numpy(), v * s)  # exact in BF16 (4 significant bits)
+        codes, scales = oracle.fp8_quantize(workloads.bits(x))
+        assert np.all(scales == np.float32(s))
+        assert np.array_equal(_fp8_decode(codes, scales), v * s)
+
+
+def test_fp8_codes_match_torch_rne_of_binary32_quotients():
+    g = torch.Generator().manual_seed(32)
+    w = (torch.randn((16, 256), generator=g) * torch.exp2(torch.randint(-8, 4, (16, 1), generator=g).float()))
+    w = w.to(torch.bfloat16)
+    codes, scales = oracle.fp8_quantize(workloads.bits(w))
+    x = w.float().numpy()
+    amax = np.abs(x).max(axis=1).astype(np.float32)
+    s = (amax / np.float32(448.0)).astype(np.float32)
+    assert np.array_equal(scales, s)
+    q = (x / s[:, None]).astype(np.float32)
+    ref = torch.from_numpy(np.clip(q, -448.0, 448.0)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(codes, ref)
+
+
+def test_fp8_zero_row_and_signs():
+    w = torch.zeros((3, 32), dtype=torch.bfloat16)
+    w[1, 3] = -0.5
+    w[2] = torch.linspace(-1, 1, 32).to(torch.bfloat16)
+    codes, scales = oracle.fp8_quantize(workloads.bits(w))
+    assert scales[0] == 0.0 and not codes[0].any()
+    assert codes[1, 3] == 0xFE and scales[1] == np.float32(0.5) / np.float32(448.0)
+    neg, pos = codes[2, :16], codes[2, 16:][::-1]
+    assert np.array_equal(neg & 0x7F, pos & 0x7F) and np.all(neg & 0x80) and not np.any(pos & 0x80)
+
+
+def test_fp8_gemv_matches_numpy_matmul():
+    g = torch.Generator().manual_seed(33)
+    w = (torch.randn((40, 96), generator=g) * 0.02).to(torch.bfloat16)
+    a = torch.randn((3, 96), generator=g).to(torch.bfloat16)
+    codes, scales = oracle.fp8_quantize(workloads.bits(w))
+    y, sabs = oracle.fp8_gemv(workloads.bits(a), codes, scales)
+    wd = _fp8_decode(codes, scales)
+    ref = a.double().numpy() @ wd.T
+    assert np.allclose(y, ref, rtol=1e-12, atol=1e-15)
+    assert np.allclose(sabs, np.abs(a.double().numpy()) @ np.abs(wd).T, rtol=1e-12)
+    y2, _ = oracle.fp8_gemv(workloads.bits(a), codes, scales, n0=7, nn=5)
+    assert np.array_equal(y2, y[:, 7:12])
