@@ -284,6 +284,7 @@ def bench_details(dev, stream, hbm, bf16):
     # batched propose: 151936 x 5120 (437.6 MB of weights > L2)
     case = workloads.propose_m8(device=dev)
     wq, _ = nd.nvfp4_quantize(case.w)
+    case_w = case.w  # kept for the FP8 variant below
     del case.w
     x = case.segments[0][0]
     prop = {}
@@ -329,6 +330,24 @@ def bench_details(dev, stream, hbm, bf16):
     ms = time_graph(chain, stream, 5) / steps
     b = gemv_bytes(5120, 10240, 1, nseg_gamma_k=10240, out_bytes_per=2, argmax=False) \
         + gemv_bytes(151936, 5120, 1, nseg_gamma_k=5120, out_bytes_per=0)
+    # FP8 weight variant of the same head (1 byte per weight + 4 per row)
+    fp8 = {}
+    w8 = nd.fp8w_quantize(case_w)
+    for m in (1, 8):
+        logits = torch.empty((m, 151936), dtype=torch.float32, device=dev)
+        idx = torch.empty((m,), dtype=torch.int32, device=dev)
+        xs = x[:m].contiguous()
+        ms8 = time_graph(lambda: nd.fp8w_gemv_argmax([(xs, None)], w8, out_logits=logits,
+                                                      out_argmax=idx, stream=stream), stream, 20)
+        b8 = 151936 * 5120 + 151936 * 4 + m * 5120 * 2 + m * 151936 * 4 + 4 * m
+        fp8[f"M{m}"] = {"us": ms8 * 1e3, "GBps": b8 / ms8 / 1e6, "frac_of_measured_hbm": b8 / ms8 / 1e6 / hbm}
+    msq = time_graph(lambda: nd.fp8w_quantize(case_w, out=w8, stream=stream), stream, 10)
+    qb8 = 2 * 151936 * 5120 * 2 + 151936 * 5120 + 151936 * 4
+    fp8["quantize"] = {"us": msq * 1e3, "GBps": qb8 / msq / 1e6,
+                       "frac_of_measured_hbm": qb8 / msq / 1e6 / hbm,
+                       "note": "BF16 read twice (second pass mostly from L1/L2) + codes + row scales"}
+    out["fp8w_propose_151936x5120"] = fp8
+    del w8, case_w
     out["chained_propose_step"] = {"us_per_step": ms * 1e3, "GBps": b / ms / 1e6,
                                    "frac_of_measured_hbm": b / ms / 1e6 / hbm,
                                    "note": "fc (embedding gathered by the previous token on "

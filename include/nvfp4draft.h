@@ -58,7 +58,12 @@ extern "C" {
 
 /* Largest activation batch of the GEMV calls (one MMA column per row). */
 #define W4A16_GEMV_MAX_M 8
-/* Largest total K of the GEMV calls (activations are staged on chip). */
+/* Largest total K of the GEMV calls (activations are staged on chip).  The
+ * FP16 activation fragments take 2 m k bytes of one CTA's shared memory next
+ * to the weight ring, so large m k combinations are refused with
+ * NVFP4_ERR_SHAPE: NVFP4 weights allow m k up to about 95 000 (every m <= 5
+ * at k = 16384; m = 8 up to k = 11 776), FP8 weights up to about 79 000
+ * (m = 8 up to k = 9 728). */
 #define W4A16_GEMV_MAX_K 16384
 /* Workspace of w4a16_gemv_argmax: W4A16_GEMV_MAX_M 64-bit keys + a counter.
  * Zero it once when allocated; every completed call leaves it zeroed. */
@@ -116,6 +121,14 @@ typedef struct w4a16_act_segment {
     const int32_t *row_index;  /* device int32 [m], 4-B aligned, or NULL      */
     int64_t index_rows;        /* rows of the table when row_index != NULL   */
 } w4a16_act_segment;
+
+/* An FP8 weight (the pages' second projection precision, see fp8w_quantize):
+ * E4M3 codes [n, k] row-major, 16-byte aligned; one FP32 scale per row. */
+typedef struct fp8w_weight {
+    const uint8_t *codes;
+    const float *row_scale;  /* device [n], 4-byte aligned */
+    int64_t n, k;            /* k a multiple of 32; n * k < 2^32 */
+} fp8w_weight;
 
 /* Execution context. */
 typedef struct nvfp4_exec {
@@ -253,6 +266,31 @@ int w4a16_gemv_argmax_noalloc(const w4a16_act_segment *seg, int nseg, int m,
  */
 int w4a16_gemm(const void *a_bf16, int64_t m, int64_t lda, const nvfp4_weight *w,
                void *c_bf16, int64_t ldc, const nvfp4_exec *ex);
+
+/*
+ * FP8 weight variant of the GEMV path: MtpHead::new in
+ * "spark_model/layers/mtp_head/new.rs" resolves gemv_fp8w's
+ * quantize_bf16_to_fp8 beside the NVFP4 pair, and its MtpQuantization::Fp8
+ * arm resolves dense_gemv_fp8w; the pages print no formula.  Plainest reading
+ * of a single quantise kernel (no separate global-absmax pass): one binary32
+ * scale per output row,
+ *     s_n = fl32(amax_n / 448),   c = E4M3_RNE_SATFINITE(fl32(x / s_n))
+ * (sign of x, all codes +0 when s_n == 0), and
+ *     y[m, n] = s_n * sum_i a[m, i] * e4m3(c[n, i])   (FP32 accumulation).
+ *
+ * fp8w_quantize -- BF16 w [n, k] (16-B aligned, k % 32 == 0) -> codes [n, k]
+ *   (16-B aligned) and row_scale [n].  One CTA per row.  Non-finite input:
+ *   results undefined, NVFP4_ERR_NONFINITE to dev_status.  No workspace.
+ * fp8w_gemv, fp8w_gemv_argmax -- the same contracts (segments, RMSNorm +
+ *   concat + gather, outputs, argmax ties, workspaces) as w4a16_gemv and
+ *   w4a16_gemv_argmax, with the FP8 weight.
+ */
+int fp8w_quantize(const void *w_bf16, int64_t n, int64_t k, uint8_t *codes, float *row_scale,
+                  const nvfp4_exec *ex);
+int fp8w_gemv(const w4a16_act_segment *seg, int nseg, int m, const fp8w_weight *w, void *y,
+              int y_dtype, int64_t ldy, const nvfp4_exec *ex);
+int fp8w_gemv_argmax(const w4a16_act_segment *seg, int nseg, int m, const fp8w_weight *w,
+                     float *logits, int64_t ld_logits, int32_t *argmax, const nvfp4_exec *ex);
 
 #ifdef __cplusplus
 }

@@ -43,7 +43,7 @@ def gemv_workspace_bytes(m: int, k: int) -> int:
     return GEMV_PREP_OFFSET + 256 + (k + 255) // 256 * 512 * m
 QUANTIZE_WS_BYTES = 16
 EXPORTED = ("nvfp4_quantize", "w4a16_gemv", "w4a16_gemv_argmax", "w4a16_gemv_argmax_ex",
-            "w4a16_gemm")
+            "w4a16_gemm", "fp8w_quantize", "fp8w_gemv", "fp8w_gemv_argmax")
 
 
 class Nvfp4Error(RuntimeError):
@@ -61,6 +61,11 @@ class _Segment(ctypes.Structure):
     _fields_ = [("x", ctypes.c_void_p), ("k_seg", ctypes.c_int64), ("ld", ctypes.c_int64),
                 ("gamma", ctypes.c_void_p), ("eps", ctypes.c_float),
                 ("row_index", ctypes.c_void_p), ("index_rows", ctypes.c_int64)]
+
+
+class _Fp8Weight(ctypes.Structure):
+    _fields_ = [("codes", ctypes.c_void_p), ("row_scale", ctypes.c_void_p),
+                ("n", ctypes.c_int64), ("k", ctypes.c_int64)]
 
 
 class _Exec(ctypes.Structure):
@@ -89,6 +94,9 @@ def load(path: str = LIB_PATH):
     L.w4a16_gemv_argmax_ex.argtypes = [P(_Segment), i32, i32, P(_Weight), vp, i64, vp, vp, vp,
                                        i64, P(_Exec)]
     L.w4a16_gemm.argtypes = [vp, i64, i64, P(_Weight), vp, i64, P(_Exec)]
+    L.fp8w_quantize.argtypes = [vp, i64, i64, vp, vp, P(_Exec)]
+    L.fp8w_gemv.argtypes = [P(_Segment), i32, i32, P(_Fp8Weight), vp, i32, i64, P(_Exec)]
+    L.fp8w_gemv_argmax.argtypes = [P(_Segment), i32, i32, P(_Fp8Weight), vp, i64, vp, P(_Exec)]
     L.w4a16_gemv_argmax_noalloc.argtypes = [P(_Segment), i32, i32, P(_Weight), vp, i64, vp, vp,
                                             vp]
     for f in EXPORTED + ("w4a16_gemv_argmax_noalloc",):
@@ -109,6 +117,18 @@ class Nvfp4Weight:
     def c(self) -> _Weight:
         return _Weight(self.packed.data_ptr(), self.scales.data_ptr(),
                        self.global_scale.data_ptr(), self.n, self.k)
+
+
+@dataclass
+class Fp8Weight:
+    """Device tensors of one per-row FP8 (E4M3) weight."""
+    codes: torch.Tensor      # uint8 [n, k]
+    row_scale: torch.Tensor  # float32 [n]
+    n: int
+    k: int
+
+    def c(self) -> _Fp8Weight:
+        return _Fp8Weight(self.codes.data_ptr(), self.row_scale.data_ptr(), self.n, self.k)
 
 
 def _stream(stream) -> int:
@@ -328,3 +348,63 @@ def w4a16_gemm(a: torch.Tensor, weight: Nvfp4Weight, out: Optional[torch.Tensor]
                            out.stride(0), ctypes.byref(ex))
     _check("w4a16_gemm", rc)
     return out
+
+
+# ------------------------------------------------------------ FP8 weights
+
+def fp8w_quantize(w: torch.Tensor, out: Optional[Fp8Weight] = None, stream=None,
+                  dev_status: Optional[torch.Tensor] = None) -> Fp8Weight:
+    """BF16 [n, k] -> per-row FP8 E4M3 codes [n, k] + row scales [n]."""
+    assert w.dtype == torch.bfloat16 and w.is_contiguous() and w.is_cuda and w.dim() == 2
+    n, k = w.shape
+    if out is None:
+        out = Fp8Weight(torch.empty((n, k), dtype=torch.uint8, device=w.device),
+                        torch.empty(n, dtype=torch.float32, device=w.device), n, k)
+    ex = _exec(stream, None, dev_status)
+    rc = load().fp8w_quantize(w.data_ptr(), n, k, out.codes.data_ptr(), out.row_scale.data_ptr(),
+                              ctypes.byref(ex))
+    _check("fp8w_quantize", rc)
+    return out
+
+
+def fp8w_gemv(segments: Sequence, weight: Fp8Weight, out_dtype=torch.float32,
+              out: Optional[torch.Tensor] = None, stream=None,
+              dev_status: Optional[torch.Tensor] = None,
+              workspace: Optional[torch.Tensor] = None, prepare: bool = True) -> torch.Tensor:
+    segs, m = _segments(segments)
+    if out is None:
+        out = torch.empty((m, weight.n), dtype=out_dtype, device=weight.codes.device)
+    dt = DTYPE_F32 if out.dtype == torch.float32 else DTYPE_BF16
+    assert out.dtype in (torch.float32, torch.bfloat16) and out.stride(1) == 1
+    if workspace is None and prepare:
+        workspace = argmax_workspace(weight.codes.device)
+    ex = _exec(stream, workspace, dev_status)
+    w = weight.c()
+    rc = load().fp8w_gemv(segs, len(segments), m, ctypes.byref(w), out.data_ptr(), dt,
+                          out.stride(0), ctypes.byref(ex))
+    _check("fp8w_gemv", rc)
+    return out
+
+
+def fp8w_gemv_argmax(segments: Sequence, weight: Fp8Weight, logits: bool = True,
+                     out_logits: Optional[torch.Tensor] = None,
+                     out_argmax: Optional[torch.Tensor] = None,
+                     workspace: Optional[torch.Tensor] = None, stream=None,
+                     dev_status: Optional[torch.Tensor] = None):
+    """Returns (logits FP32 [m, n] or None, argmax int32 [m])."""
+    segs, m = _segments(segments)
+    dev = weight.codes.device
+    if logits and out_logits is None:
+        out_logits = torch.empty((m, weight.n), dtype=torch.float32, device=dev)
+    if out_argmax is None:
+        out_argmax = torch.empty(m, dtype=torch.int32, device=dev)
+    if workspace is None:
+        workspace = argmax_workspace(dev)
+    ex = _exec(stream, workspace, dev_status)
+    w = weight.c()
+    rc = load().fp8w_gemv_argmax(segs, len(segments), m, ctypes.byref(w),
+                                 out_logits.data_ptr() if out_logits is not None else None,
+                                 out_logits.stride(0) if out_logits is not None else 0,
+                                 out_argmax.data_ptr(), ctypes.byref(ex))
+    _check("fp8w_gemv_argmax", rc)
+    return out_logits, out_argmax

@@ -72,6 +72,14 @@ int check_weight(const nvfp4_weight* w) {
   return NVFP4_OK;
 }
 
+int check_fp8_weight(const fp8w_weight* w) {
+  if (w == nullptr || w->codes == nullptr || w->row_scale == nullptr) return NVFP4_ERR_NULL;
+  if (w->n < 1 || w->k < 32 || w->k % 32 != 0) return NVFP4_ERR_SHAPE;
+  if (w->n * w->k >= (int64_t)1 << 32) return NVFP4_ERR_SHAPE;  // 32-bit offsets
+  if (!aligned16(w->codes) || (reinterpret_cast<uintptr_t>(w->row_scale) & 3u)) return NVFP4_ERR_ALIGN;
+  return NVFP4_OK;
+}
+
 int check_segments(const w4a16_act_segment* seg, int nseg, int m, int64_t k) {
   if (seg == nullptr) return NVFP4_ERR_NULL;
   if (nseg < 1 || nseg > 2) return NVFP4_ERR_SHAPE;
@@ -122,6 +130,7 @@ bool encode_tiled(CUtensorMap* map, CUtensorMapDataType type, cuuint32_t rank, v
 namespace {
 
 using nvfp4::aligned16;
+using nvfp4::check_fp8_weight;
 using nvfp4::check_segments;
 using nvfp4::check_weight;
 
@@ -165,7 +174,7 @@ int w4a16_gemv(const w4a16_act_segment* seg, int nseg, int m, const nvfp4_weight
   if (ldy < w->n) return NVFP4_ERR_SHAPE;
   const uintptr_t ya = reinterpret_cast<uintptr_t>(y);
   if ((y_dtype == NVFP4_DTYPE_F32 && (ya & 3u)) || (ya & 1u)) return NVFP4_ERR_ALIGN;
-  return launch_gemv(seg, nseg, m, w, y, y_dtype, ldy, false, nullptr,
+  return launch_gemv(seg, nseg, m, ref_of(w), y, y_dtype, ldy, false, nullptr,
                      ex != nullptr ? ex->workspace : nullptr, ex != nullptr ? ex->workspace_bytes : 0,
                      status_of(ex), stream_of(ex));
 }
@@ -185,7 +194,7 @@ int w4a16_gemv_argmax(const w4a16_act_segment* seg, int nseg, int m, const nvfp4
   if (ex == nullptr || ex->workspace == nullptr || ex->workspace_bytes < W4A16_ARGMAX_WS_BYTES ||
       !aligned16(ex->workspace))
     return NVFP4_ERR_WORKSPACE;
-  return launch_gemv(seg, nseg, m, w, logits, NVFP4_DTYPE_F32, ld_logits, true, argmax,
+  return launch_gemv(seg, nseg, m, ref_of(w), logits, NVFP4_DTYPE_F32, ld_logits, true, argmax,
                      ex->workspace, ex->workspace_bytes, status_of(ex), stream_of(ex));
 }
 
@@ -208,7 +217,7 @@ int w4a16_gemv_argmax_ex(const w4a16_act_segment* seg, int nseg, int m, const nv
   if (ex == nullptr || ex->workspace == nullptr || ex->workspace_bytes < W4A16_ARGMAX_EX_WS_BYTES ||
       !aligned16(ex->workspace))
     return NVFP4_ERR_WORKSPACE;
-  return launch_gemv(seg, nseg, m, w, logits, NVFP4_DTYPE_F32, ld_logits, true, argmax,
+  return launch_gemv(seg, nseg, m, ref_of(w), logits, NVFP4_DTYPE_F32, ld_logits, true, argmax,
                      ex->workspace, ex->workspace_bytes, status_of(ex), stream_of(ex), logprob, mask,
                      ld_mask);
 }
@@ -225,6 +234,50 @@ int w4a16_gemm(const void* a_bf16, int64_t m, int64_t lda, const nvfp4_weight* w
     return NVFP4_ERR_ALIGN;
   return launch_gemm(a_bf16, m, lda, w, c_bf16, ldc, ex ? ex->workspace : nullptr,
                      ex ? ex->workspace_bytes : 0, status_of(ex), stream_of(ex));
+}
+
+int fp8w_quantize(const void* w_bf16, int64_t n, int64_t k, uint8_t* codes, float* row_scale,
+                  const nvfp4_exec* ex) {
+  if (w_bf16 == nullptr || codes == nullptr || row_scale == nullptr) return NVFP4_ERR_NULL;
+  if (n < 1 || k < 32 || k % 32 != 0 || n * k >= (int64_t)1 << 32) return NVFP4_ERR_SHAPE;
+  if (!aligned16(w_bf16) || !aligned16(codes) || (reinterpret_cast<uintptr_t>(row_scale) & 3u))
+    return NVFP4_ERR_ALIGN;
+  return launch_fp8_quantize(w_bf16, n, k, codes, row_scale, status_of(ex), stream_of(ex));
+}
+
+int fp8w_gemv(const w4a16_act_segment* seg, int nseg, int m, const fp8w_weight* w, void* y,
+              int y_dtype, int64_t ldy, const nvfp4_exec* ex) {
+  int rc = check_fp8_weight(w);
+  if (rc) return rc;
+  rc = check_segments(seg, nseg, m, w->k);
+  if (rc) return rc;
+  if (y == nullptr) return NVFP4_ERR_NULL;
+  if (y_dtype != NVFP4_DTYPE_F32 && y_dtype != NVFP4_DTYPE_BF16) return NVFP4_ERR_DTYPE;
+  if (ldy < w->n) return NVFP4_ERR_SHAPE;
+  const uintptr_t ya = reinterpret_cast<uintptr_t>(y);
+  if ((y_dtype == NVFP4_DTYPE_F32 && (ya & 3u)) || (ya & 1u)) return NVFP4_ERR_ALIGN;
+  return launch_gemv(seg, nseg, m, ref_of(w), y, y_dtype, ldy, false, nullptr,
+                     ex != nullptr ? ex->workspace : nullptr, ex != nullptr ? ex->workspace_bytes : 0,
+                     status_of(ex), stream_of(ex));
+}
+
+int fp8w_gemv_argmax(const w4a16_act_segment* seg, int nseg, int m, const fp8w_weight* w,
+                     float* logits, int64_t ld_logits, int32_t* argmax, const nvfp4_exec* ex) {
+  int rc = check_fp8_weight(w);
+  if (rc) return rc;
+  rc = check_segments(seg, nseg, m, w->k);
+  if (rc) return rc;
+  if (argmax == nullptr) return NVFP4_ERR_NULL;
+  if ((reinterpret_cast<uintptr_t>(argmax) & 3u) ||
+      (logits != nullptr && (reinterpret_cast<uintptr_t>(logits) & 3u)))
+    return NVFP4_ERR_ALIGN;
+  if (logits != nullptr && ld_logits < w->n) return NVFP4_ERR_SHAPE;
+  if (w->n > 0x7FFFFFFFLL) return NVFP4_ERR_SHAPE;
+  if (ex == nullptr || ex->workspace == nullptr || ex->workspace_bytes < W4A16_ARGMAX_WS_BYTES ||
+      !aligned16(ex->workspace))
+    return NVFP4_ERR_WORKSPACE;
+  return launch_gemv(seg, nseg, m, ref_of(w), logits, NVFP4_DTYPE_F32, ld_logits, true,
+                     argmax, ex->workspace, ex->workspace_bytes, status_of(ex), stream_of(ex));
 }
 
 }  // extern "C"

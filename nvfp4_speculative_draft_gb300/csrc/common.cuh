@@ -54,6 +54,7 @@ bool encode_tiled(CUtensorMap* map, CUtensorMapDataType type, cuuint32_t rank, v
 // Host-side argument checks shared by the entry points (status codes of
 // nvfp4draft.h).
 int check_weight(const nvfp4_weight* w);
+int check_fp8_weight(const fp8w_weight* w);
 int check_segments(const w4a16_act_segment* seg, int nseg, int m, int64_t k);
 
 }  // namespace nvfp4
@@ -62,7 +63,25 @@ int check_segments(const w4a16_act_segment* seg, int nseg, int m, int64_t k);
 int launch_quantize(const void* w, int64_t n, int64_t k, uint8_t* packed, uint8_t* scales,
                     float* global_scale, uint32_t* amax_word, int32_t* dev_status,
                     cudaStream_t stream);
-int launch_gemv(const w4a16_act_segment* seg, int nseg, int m, const nvfp4_weight* w,
+// The GEMV's view of a weight: NVFP4 (packed codes, block scales, global
+// scale) or FP8 (E4M3 codes, one scale per row).
+struct WeightRef {
+  const uint8_t* codes;
+  const uint8_t* scales;
+  const float* gscale;
+  const float* row_scale;
+  int64_t n, k;
+  bool fp8;
+};
+inline WeightRef ref_of(const nvfp4_weight* w) {
+  return WeightRef{w->packed, w->scales, w->global_scale, nullptr, w->n, w->k, false};
+}
+inline WeightRef ref_of(const fp8w_weight* w) {
+  return WeightRef{w->codes, nullptr, nullptr, w->row_scale, w->n, w->k, true};
+}
+int launch_fp8_quantize(const void* w, int64_t n, int64_t k, uint8_t* codes, float* row_scale,
+                        int32_t* dev_status, cudaStream_t stream);
+int launch_gemv(const w4a16_act_segment* seg, int nseg, int m, const WeightRef& w,
                 void* y, int y_dtype, int64_t ldy, bool want_argmax, int32_t* argmax,
                 void* workspace, size_t workspace_bytes, int32_t* dev_status, cudaStream_t stream,
                 float* logprob = nullptr, const int32_t* mask = nullptr, int64_t ld_mask = 0);

@@ -47,6 +47,10 @@ namespace {
 constexpr int kChunk = 128;       // K elements per chunk (64 packed bytes per row)
 constexpr int kItem = 2;          // chunks per stage (one TMA box of 16 rows x 128 bytes)
 constexpr int kStageBytes = 16 * 64 * kItem;
+// FP8 weights: one ring stage is 16 rows x 256 bytes (two 128-element chunks
+// of codes), so each row segment a TMA box reads is 256 contiguous bytes.
+constexpr int kStageBytesFp8 = 16 * 256;
+__host__ __device__ constexpr int stage_bytes(bool fp8) { return fp8 ? kStageBytesFp8 : kStageBytes; }
 // TMA stages per warp (two two-chunk boxes: 4 KB in flight per warp; deeper
 // rings measured no faster).
 __host__ __device__ constexpr int ring_stages(int, int) { return 2; }
@@ -63,8 +67,9 @@ struct GemvParams {
   float eps[2];
   int nseg;
   int m;
-  const uint8_t* scales;
-  const float* gscale;
+  const uint8_t* scales;     // NVFP4: E4M3 block scales [n, k/16]
+  const float* gscale;       // NVFP4: global scale
+  const float* row_scale;    // FP8: per-row scales [n]
   int64_t n, k;
   void* y;
   int y_dtype;
@@ -202,6 +207,34 @@ __device__ __forceinline__ void chunk_mma(float (&acc)[4], const uint4& qg, cons
     const uint2 b1 = bfrag[(2 * w + 1) * BSTRIDE];
     mma_f16_16816(acc, f16x2_mul(g2, sG), f16x2_mul(h2, sH), f16x2_mul(g3, sG),
                   f16x2_mul(h3, sH), b1.x, b1.y);
+  }
+}
+
+// FP8 weights: the lane's 32 codes of row g (g + 8) for one 128-element
+// chunk are words W0..W7 of qg0, qg1 (qh0, qh1); MMA q takes word Wq (k
+// elements 4q .. 4q+3 of the lane's 32, the same order as the NVFP4 path, so
+// the activation fragments are shared).  No block scales: the row scale
+// multiplies the finished sum.
+__device__ __forceinline__ void e4m3_word_to_f16(uint32_t q, uint32_t& lo, uint32_t& hi) {
+  asm("{\n .reg .b16 a, b;\n mov.b32 {a, b}, %2;\n cvt.rn.f16x2.e4m3x2 %0, a;\n"
+      " cvt.rn.f16x2.e4m3x2 %1, b;\n}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(q));
+}
+
+template <int BSTRIDE>
+__device__ __forceinline__ void chunk_mma_fp8(float (&acc)[4], const uint4& qg0, const uint4& qg1,
+                                              const uint4& qh0, const uint4& qh1,
+                                              const uint2* bfrag) {
+  const uint32_t wg[8] = {qg0.x, qg0.y, qg0.z, qg0.w, qg1.x, qg1.y, qg1.z, qg1.w};
+  const uint32_t wh[8] = {qh0.x, qh0.y, qh0.z, qh0.w, qh1.x, qh1.y, qh1.z, qh1.w};
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    uint32_t g0, g1, h0, h1;
+    e4m3_word_to_f16(wg[q], g0, g1);
+    e4m3_word_to_f16(wh[q], h0, h1);
+    const uint2 b = bfrag[q * BSTRIDE];
+    mma_f16_16816(acc, g0, h0, g1, h1, b.x, b.y);
   }
 }
 
@@ -363,6 +396,9 @@ __device__ __noinline__ void build_fragments(const GemvParams& p, uint2* bfrag, 
   const int gpr = p.nchunks * (kChunk / 8);  // 8-element groups per row
   for (int r = r0; r < r0 + nrows; ++r) {
     const float sc = row_scale_pow2(rowmax[r], false);
+    // the row's base in each segment, resolved once (a gathered row reads its index here)
+    const __nv_bfloat16* xr0 = seg_row(p, 0, r);
+    const __nv_bfloat16* xr1 = p.nseg == 2 ? seg_row(p, 1, r) : xr0;
 #pragma unroll 2
     for (int q = tid; q < gpr; q += kThreads) {
       const int kk = q * 8;
@@ -370,7 +406,7 @@ __device__ __noinline__ void build_fragments(const GemvParams& p, uint2* bfrag, 
       const int s = (p.nseg == 2 && kk >= p.kseg[0]) ? 1 : 0;
       const int ko = kk - (s ? (int)p.kseg[0] : 0);
       if (kk < p.k && NVFP4_GUARD(ko >= 0 && ko + 8 <= p.kseg[s], 2, p.dev_status)) {
-        const uint4 v = *reinterpret_cast<const uint4*>(seg_row(p, s, r) + ko);
+        const uint4 v = *reinterpret_cast<const uint4*>((s ? xr1 : xr0) + ko);
         a[0] = v.x; a[1] = v.y; a[2] = v.z; a[3] = v.w;
         if (p.gamma[s] != nullptr) {
           const uint4 gv = *reinterpret_cast<const uint4*>(p.gamma[s] + ko);
@@ -434,7 +470,7 @@ __device__ __forceinline__ void bar_arrive(int id, int count) {
 // a contiguous range of its k chunks (split K); a CTA takes WARPS/ks tiles at a
 // time and strides over the tiles persistently.  Each warp streams its
 // (tile, chunk) items in order through its TMA ring, across tile boundaries.
-template <int M, int WARPS>
+template <int M, int WARPS, bool FP8>
 __global__ void __launch_bounds__(WARPS * 32, WARPS >= 16 ? 2 : 1)
 gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ GemvParams p) {
   constexpr int BSTRIDE = 4 * M;
@@ -455,12 +491,15 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
   const int tpc = kWarps / ks;  // tiles per CTA iteration
   const int slot = warp / ks, kpart = warp % ks;
   // this warp's items (pairs of chunks) [ib, ib + L) of every tile
-  const int nitems = (p.nchunks + kItem - 1) / kItem;
+  constexpr int kIt = kItem;               // chunks per ring stage
+  constexpr int kStage = stage_bytes(FP8);  // 16 rows x 128 (NVFP4) or 256 (FP8) bytes
+  constexpr int kRowBytes = kStage / 16;
+  const int nitems = (p.nchunks + kIt - 1) / kIt;
   const int ib = (int)((int64_t)kpart * nitems / ks);
   const int L = (int)((int64_t)(kpart + 1) * nitems / ks) - ib;
   const int64_t ngroups = (p.ntiles + tpc - 1) / tpc;
   const int n_iter = blockIdx.x < ngroups ? (int)((ngroups - 1 - blockIdx.x) / gridDim.x) + 1 : 0;
-  const uint32_t ring = base + p.off_ring + (uint32_t)warp * (kRing * kStageBytes);
+  const uint32_t ring = base + p.off_ring + (uint32_t)warp * (kRing * kStage);
   const uint32_t bars = base + p.off_bar + (uint32_t)warp * (kRing * 8);
   // chunks c with 128c + 32t < k hold this lane's data (scales past k read 0)
   const int cmax = (int)((p.k - 32 * t + kChunk - 1) / kChunk);
@@ -487,22 +526,26 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
     int64_t r0 = tile * 16 + g, r1 = r0 + 8;
     r0 = r0 < p.n ? r0 : p.n - 1;  // rows past n: any valid scale (their codes read as 0)
     r1 = r1 < p.n ? r1 : p.n - 1;
-    sp0 = reinterpret_cast<const uint16_t*>(p.scales + r0 * (p.k / 16)) + t;
-    sp1 = reinterpret_cast<const uint16_t*>(p.scales + r1 * (p.k / 16)) + t;
+    if constexpr (!FP8) {
+      sp0 = reinterpret_cast<const uint16_t*>(p.scales + r0 * (p.k / 16)) + t;
+      sp1 = reinterpret_cast<const uint16_t*>(p.scales + r1 * (p.k / 16)) + t;
+    }
   };
   const int total = n_iter * L;
   uint32_t sreg[kRing][kItem];  // block-scale pairs of rows g, g+8 (low / high 16 bits)
   if (total > 0) set_tile(0);
   auto issue = [&](int i) {
-    const int c0 = (ib + lc) * kItem;
+    const int c0 = (ib + lc) * kIt;
     if (lane == 0) {
-      mbar_arrive_expect_tx(bars + 8 * i, kStageBytes);
-      tma_load_2d(ring + i * kStageBytes, &tmap_w, c0 * 64, ltile16, bars + 8 * i);
+      mbar_arrive_expect_tx(bars + 8 * i, kStage);
+      tma_load_2d(ring + i * kStage, &tmap_w, (ib + lc) * kRowBytes, ltile16, bars + 8 * i);
     }
+    if constexpr (!FP8) {
 #pragma unroll
-    for (int j = 0; j < kItem; ++j) {
-      const int c = c0 + j;
-      sreg[i][j] = c < cmax ? ((uint32_t)__ldg(sp0 + 4 * c) | ((uint32_t)__ldg(sp1 + 4 * c) << 16)) : 0u;
+      for (int j = 0; j < kItem; ++j) {
+        const int c = c0 + j;
+        sreg[i][j] = c < cmax ? ((uint32_t)__ldg(sp0 + 4 * c) | ((uint32_t)__ldg(sp1 + 4 * c) << 16)) : 0u;
+      }
     }
     if (++lc == L) {
       lc = 0;
@@ -521,7 +564,7 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
       const int64_t tile = ((int64_t)blockIdx.x + (int64_t)pt * gridDim.x) * tpc + slot;
       asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global [%0, {%1, %2}];" ::"l"(
                        reinterpret_cast<uint64_t>(&tmap_w)),
-                   "r"((ib + pc) * kItem * 64), "r"((int)(tile * 16))
+                   "r"((ib + pc) * kRowBytes), "r"((int)(tile * 16))
                    : "memory");
       if (++pc == L) { pc = 0; ++pt; }
     }
@@ -558,7 +601,7 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
   }
   __syncthreads();
 
-  const float gsc = __ldg(p.gscale);
+  const float gsc = FP8 ? 1.0f : __ldg(p.gscale);
   // inverse activation scales of this lane's two batch columns (2t, 2t+1)
   const unsigned int* rowmax = reinterpret_cast<const unsigned int*>(rms + kSmallRowmax);
   const float inv0 = row_scale_pow2(rowmax[min(2 * t, M - 1)], true);
@@ -571,11 +614,18 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
 
   // Grammar mask: the 16 rows of a tile share one 32-bit mask word per batch
   // column; the consumer warp loads the next tile's words during this tile.
+  // FP8: the row scales of the consumer's rows g, g + 8, loaded the same way.
   uint32_t mword[2] = {0xFFFFFFFFu, 0xFFFFFFFFu};
+  float rsc[2] = {0.f, 0.f};
   auto load_mask = [&](int it) {
-    if (p.mask == nullptr) return;
+    if (!FP8 && p.mask == nullptr) return;
     const int64_t tile = ((int64_t)blockIdx.x + (int64_t)it * gridDim.x) * tpc + slot;
     if (it >= n_iter || tile >= p.ntiles) return;
+    if constexpr (FP8) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) rsc[h] = __ldg(p.row_scale + min(tile * 16 + g + 8 * h, p.n - 1));
+    }
+    if (p.mask == nullptr) return;
 #pragma unroll
     for (int e = 0; e < 2; ++e)
       mword[e] = __ldg(reinterpret_cast<const uint32_t*>(p.mask) +
@@ -612,7 +662,7 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
         for (int e = 0; e < 2; ++e) {
           const int mm = 2 * t + e;
           if (mm >= M) continue;
-          const float v = (acc[2 * h + e] * (e ? inv1 : inv0)) * gsc;
+          const float v = (acc[2 * h + e] * (e ? inv1 : inv0)) * (FP8 ? rsc[h] : gsc);
           if (p.y != nullptr &&
               NVFP4_GUARD(mm < M && rows[h] < p.n && rows[h] < p.ldy, 6, p.dev_status)) {
             if (p.y_dtype == NVFP4_DTYPE_F32)
@@ -645,15 +695,28 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
       const int q = q0 + i;
       if (q < total) {
         if (alive) alive = mbar_wait(bars + 8 * i, (uint32_t)(q / kRing) & 1u, p.dev_status);
-        const unsigned char* st = smem + (ring - base) + i * kStageBytes;
-        const uint2* bq = bbase + (int64_t)(8 * kItem * (ib + cc)) * BSTRIDE;
+        const unsigned char* st = smem + (ring - base) + i * kStage;
+        const uint2* bq = bbase + (int64_t)(8 * kIt * (ib + cc)) * BSTRIDE;
+        if constexpr (FP8) {  // box rows are two 128-element chunks of codes
 #pragma unroll
-        for (int j = 0; j < kItem; ++j) {  // box rows are 64 * kItem bytes
-          const uint4 qg = *reinterpret_cast<const uint4*>(st + g * (64 * kItem) + j * 64 + t * 16);
-          const uint4 qh =
-              *reinterpret_cast<const uint4*>(st + (g + 8) * (64 * kItem) + j * 64 + t * 16);
-          const uint32_t s2 = sreg[i][j];
-          chunk_mma<BSTRIDE>(acc, qg, qh, s2 & 0xFFFFu, s2 >> 16, bq + 8 * j * BSTRIDE);
+          for (int j = 0; j < kItem; ++j) {
+            const unsigned char* rg = st + g * kRowBytes + j * 128 + t * 32;
+            const unsigned char* rh = st + (g + 8) * kRowBytes + j * 128 + t * 32;
+            const uint4 qg0 = *reinterpret_cast<const uint4*>(rg);
+            const uint4 qg1 = *reinterpret_cast<const uint4*>(rg + 16);
+            const uint4 qh0 = *reinterpret_cast<const uint4*>(rh);
+            const uint4 qh1 = *reinterpret_cast<const uint4*>(rh + 16);
+            chunk_mma_fp8<BSTRIDE>(acc, qg0, qg1, qh0, qh1, bq + 8 * j * BSTRIDE);
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < kItem; ++j) {  // box rows are 64 * kItem bytes
+            const uint4 qg = *reinterpret_cast<const uint4*>(st + g * (64 * kItem) + j * 64 + t * 16);
+            const uint4 qh =
+                *reinterpret_cast<const uint4*>(st + (g + 8) * (64 * kItem) + j * 64 + t * 16);
+            const uint32_t s2 = sreg[i][j];
+            chunk_mma<BSTRIDE>(acc, qg, qh, s2 & 0xFFFFu, s2 >> 16, bq + 8 * j * BSTRIDE);
+          }
         }
         __syncwarp();  // every lane is done with stage i before it is refilled
         if (q + kRing < total) issue(i);
@@ -789,17 +852,17 @@ PrepFn prep_for(int m) {
   }
 }
 
-template <int WARPS>
+template <int WARPS, bool FP8>
 KernelFn kernel_for(int m) {
   switch (m) {
-    case 1: return gemv_kernel<1, WARPS>;
-    case 2: return gemv_kernel<2, WARPS>;
-    case 3: return gemv_kernel<3, WARPS>;
-    case 4: return gemv_kernel<4, WARPS>;
-    case 5: return gemv_kernel<5, WARPS>;
-    case 6: return gemv_kernel<6, WARPS>;
-    case 7: return gemv_kernel<7, WARPS>;
-    default: return gemv_kernel<8, WARPS>;
+    case 1: return gemv_kernel<1, WARPS, FP8>;
+    case 2: return gemv_kernel<2, WARPS, FP8>;
+    case 3: return gemv_kernel<3, WARPS, FP8>;
+    case 4: return gemv_kernel<4, WARPS, FP8>;
+    case 5: return gemv_kernel<5, WARPS, FP8>;
+    case 6: return gemv_kernel<6, WARPS, FP8>;
+    case 7: return gemv_kernel<7, WARPS, FP8>;
+    default: return gemv_kernel<8, WARPS, FP8>;
   }
 }
 
@@ -808,7 +871,7 @@ struct Layout {
   size_t bytes;  // dynamic shared memory to request (includes 1 KB alignment slack)
 };
 
-Layout layout_for(int warps, int m, int nchunks) {
+Layout layout_for(int warps, int m, int nchunks, bool fp8) {
   const int kRing = ring_stages(m, warps);
   Layout l;
   size_t off = (size_t)nchunks * 8 * 4 * m * sizeof(uint2);  // B fragments
@@ -821,7 +884,7 @@ Layout layout_for(int warps, int m, int nchunks) {
   off += (size_t)warps * 8 * sizeof(unsigned long long) + (size_t)warps * 8 * sizeof(float2);
   off = (off + 1023) & ~(size_t)1023;
   l.off_ring = (uint32_t)off;
-  off += (size_t)warps * kRing * kStageBytes;
+  off += (size_t)warps * kRing * stage_bytes(fp8);
   l.off_bar = (uint32_t)off;
   off += (size_t)warps * kRing * 8 + 8;  // ring barriers + the fragment-copy barrier
   l.bytes = off + 1024;
@@ -830,7 +893,7 @@ Layout layout_for(int warps, int m, int nchunks) {
 
 }  // namespace
 
-int launch_gemv(const w4a16_act_segment* seg, int nseg, int m, const nvfp4_weight* w, void* y,
+int launch_gemv(const w4a16_act_segment* seg, int nseg, int m, const WeightRef& w, void* y,
                 int y_dtype, int64_t ldy, bool want_argmax, int32_t* argmax, void* workspace,
                 size_t workspace_bytes, int32_t* dev_status, cudaStream_t stream, float* logprob,
                 const int32_t* mask, int64_t ld_mask) {
@@ -846,10 +909,11 @@ int launch_gemv(const w4a16_act_segment* seg, int nseg, int m, const nvfp4_weigh
   }
   p.nseg = nseg;
   p.m = m;
-  p.scales = w->scales;
-  p.gscale = w->global_scale;
-  p.n = w->n;
-  p.k = w->k;
+  p.scales = w.scales;
+  p.gscale = w.gscale;
+  p.row_scale = w.row_scale;
+  p.n = w.n;
+  p.k = w.k;
   p.y = y;
   p.y_dtype = y_dtype;
   p.ldy = ldy;
@@ -863,24 +927,36 @@ int launch_gemv(const w4a16_act_segment* seg, int nseg, int m, const nvfp4_weigh
     p.lse = reinterpret_cast<float2*>(reinterpret_cast<char*>(workspace) + 128);
   }
   p.dev_status = dev_status;
-  p.ntiles = nvfp4::cdiv(w->n, 16);
-  // round k's chunks up to whole items: the padding chunk's activations are
-  // zero and its weights arrive as zeros (TMA bounds fill)
-  p.nchunks = (int)(nvfp4::cdiv(nvfp4::cdiv(w->k, kChunk), kItem) * kItem);
+  p.ntiles = nvfp4::cdiv(w.n, 16);
+  // Round k's chunks up to whole items (two chunks per ring stage); the
+  // padding chunk's activations are zero and its weights arrive as zeros (TMA
+  // bounds fill).
+  const int item_chunks = kItem;
+  p.nchunks = (int)(nvfp4::cdiv(nvfp4::cdiv(w.k, kChunk), item_chunks) * item_chunks);
+  const int nitems = p.nchunks / item_chunks;
   if (p.ntiles * 16 > 0x7FFFFFFFLL) return NVFP4_ERR_SHAPE;  // TMA row coordinate
 
   // 16-warp CTAs when their shared memory fits, else 8-warp CTAs.
   int warps = 16;
-  Layout lay = layout_for(16, m, p.nchunks);
-  KernelFn fn = kernel_for<16>(m);
+  Layout lay = layout_for(16, m, p.nchunks, w.fp8);
+  KernelFn fn = w.fp8 ? kernel_for<16, true>(m) : kernel_for<16, false>(m);
   int occ = nvfp4::occupancy(reinterpret_cast<const void*>(fn), 16 * 32, lay.bytes);
   if (occ < 1) {
     warps = 8;
-    lay = layout_for(8, m, p.nchunks);
-    fn = kernel_for<8>(m);
+    lay = layout_for(8, m, p.nchunks, w.fp8);
+    fn = w.fp8 ? kernel_for<8, true>(m) : kernel_for<8, false>(m);
     occ = nvfp4::occupancy(reinterpret_cast<const void*>(fn), 8 * 32, lay.bytes);
   }
-  if (occ < 1) return NVFP4_ERR_CUDA;
+  if (occ < 1) {
+    // the activation fragments (2 m k bytes) plus the weight ring do not fit
+    // one CTA's shared memory: a size limit of the call, not a launch failure
+    int dev = 0, optin = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) == cudaSuccess &&
+        lay.bytes > (size_t)optin)
+      return NVFP4_ERR_SHAPE;
+    return NVFP4_ERR_CUDA;
+  }
   p.off_red = lay.off_red;
   p.off_small = lay.off_small;
   p.off_kred = lay.off_kred;
@@ -888,11 +964,12 @@ int launch_gemv(const w4a16_act_segment* seg, int nseg, int m, const nvfp4_weigh
   p.off_bar = lay.off_bar;
 
   CUtensorMap tmap;
-  const cuuint64_t dims[2] = {(cuuint64_t)(w->k / 2), (cuuint64_t)w->n};
-  const cuuint64_t strides[1] = {(cuuint64_t)(w->k / 2)};
-  const cuuint32_t box[2] = {64 * kItem, 16};
+  const int64_t row_bytes = w.fp8 ? w.k : w.k / 2;
+  const cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)w.n};
+  const cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+  const cuuint32_t box[2] = {(cuuint32_t)(stage_bytes(w.fp8) / 16), 16};  // one ring stage
   const cuuint32_t estr[2] = {1, 1};
-  if (!nvfp4::encode_tiled(&tmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(w->packed),
+  if (!nvfp4::encode_tiled(&tmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(w.codes),
                            dims, strides, box, estr, CU_TENSOR_MAP_SWIZZLE_NONE))
     return NVFP4_ERR_CUDA;
 
@@ -904,7 +981,7 @@ int launch_gemv(const w4a16_act_segment* seg, int nseg, int m, const nvfp4_weigh
   // are 1, 4, 8, 16 (at most 4 tile groups per CTA share its named barriers).
   int ks = 1;
   while (ks < warps && nvfp4::cdiv(p.ntiles, warps / ks) < slots &&
-         p.nchunks / kItem / (2 * ks) >= 2)
+         nitems / (2 * ks) >= 2)
     ks = ks == 1 ? 4 : 2 * ks;
   if (ks > 1 && warps / ks > 4) ks = warps / 4;
   p.ks = ks;
@@ -919,7 +996,7 @@ int launch_gemv(const w4a16_act_segment* seg, int nseg, int m, const nvfp4_weigh
   // CTA copies its result.  At m = 1 the per-CTA prologue is short and mostly
   // hidden behind the first weight loads; the extra launch costs more.
   const bool prep = m >= 2 && workspace != nullptr &&
-                    workspace_bytes >= W4A16_GEMV_WS_BYTES(m, w->k) && nvfp4::aligned16(workspace);
+                    workspace_bytes >= W4A16_GEMV_WS_BYTES(m, w.k) && nvfp4::aligned16(workspace);
   if (prep) {
     char* ws = reinterpret_cast<char*>(workspace);
     unsigned int* rowmax = reinterpret_cast<unsigned int*>(ws + W4A16_GEMV_PREP_OFFSET);

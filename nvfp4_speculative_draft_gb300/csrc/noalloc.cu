@@ -65,6 +65,6 @@ extern "C" int w4a16_gemv_argmax_noalloc(const w4a16_act_segment* seg, int nseg,
   if (rc) return rc;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(scratch, 0, W4A16_ARGMAX_WS_BYTES, st) != cudaSuccess) return NVFP4_ERR_CUDA;
-  return launch_gemv(seg, nseg, m, w, logits, NVFP4_DTYPE_F32, ld_logits, true, argmax, scratch,
+  return launch_gemv(seg, nseg, m, ref_of(w), logits, NVFP4_DTYPE_F32, ld_logits, true, argmax, scratch,
                      W4A16_ARGMAX_WS_BYTES, dev_status, st);
 }

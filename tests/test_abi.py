@@ -139,6 +139,26 @@ def test_gather_segment_argument_checks(L):
     assert f(no_rows, 1, 1, ctypes.byref(w), 0x6000, 0, 256, ctypes.byref(ex)) == 2
 
 
+def test_fp8w_argument_checks(L):
+    import nvfp4_speculative_draft_gb300 as nd
+    ex = nd._Exec(None, None, 0, None)
+    q = L.fp8w_quantize
+    assert q(None, 4, 64, 0x2000, 0x3000, ctypes.byref(ex)) == 1
+    assert q(0x1000, 4, 48, 0x2000, 0x3000, ctypes.byref(ex)) == 2
+    assert q(0x1008, 4, 64, 0x2000, 0x3000, ctypes.byref(ex)) == 3
+    assert q(0x1000, 4, 64, 0x2000, 0x3002, ctypes.byref(ex)) == 3
+    seg = (nd._Segment * 1)(_seg(nd))
+    w = nd._Fp8Weight(0x1000, 0x3000, 256, 512)
+    f = L.fp8w_gemv
+    assert f(seg, 1, 1, ctypes.byref(nd._Fp8Weight(0x1000, None, 256, 512)), 0x6000, 0, 256,
+             ctypes.byref(ex)) == 1
+    assert f(seg, 1, 1, ctypes.byref(nd._Fp8Weight(0x1004, 0x3000, 256, 512)), 0x6000, 0, 256,
+             ctypes.byref(ex)) == 3
+    assert f(seg, 1, 1, ctypes.byref(w), 0x6000, 0, 200, ctypes.byref(ex)) == 2
+    a = L.fp8w_gemv_argmax
+    assert a(seg, 1, 1, ctypes.byref(w), 0x6000, 256, 0x7000, ctypes.byref(ex)) == 4
+
+
 def test_gemm_argument_checks(L):
     import nvfp4_speculative_draft_gb300 as nd
     ex = nd._Exec(None, None, 0, None)

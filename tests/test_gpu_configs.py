@@ -223,3 +223,31 @@ def test_prefill_gemm_config_sampled(dev):
         got = out.float().cpu().numpy()[rows, cols].astype(np.float64)
         bad = np.abs(got - exact) > TOL_REL * sabs + TOL_ABS + np.abs(exact) * 2.0 ** -8
         assert not bad.any(), f"{int(bad.sum())} sampled outputs out of tolerance"
+
+
+def test_fp8_propose_full_width(dev):
+    """FP8 weight variant on the 151936 x 5120 head: per-row codes and scales
+    bit-exact on sampled rows, M=1 logits over every row and the argmax."""
+    m = nd()
+    case = workloads.propose_m8(device=dev)
+    wq = m.fp8w_quantize(case.w)
+    wb = workloads.bits(case.w)
+    rng = np.random.default_rng(13)
+    rows = np.unique(np.concatenate([rng.integers(0, 151936, 2000), [0, 151935]]))
+    codes_s, scales_s = oracle.fp8_quantize(wb, rows)
+    del wb
+    torch.cuda.synchronize()
+    assert np.array_equal(wq.row_scale.cpu().numpy()[rows], scales_s)
+    assert np.array_equal(wq.codes[torch.from_numpy(rows).to(dev)].cpu().numpy(), codes_s)
+    codes, scales = wq.codes.cpu().numpy(), wq.row_scale.cpu().numpy()
+    x = case.segments[0][0][:1].contiguous()
+    logits, idx = m.fp8w_gemv_argmax([(x, None)], wq)
+    torch.cuda.synchronize()
+    a = workloads.bits(x)
+    bounds = np.linspace(0, 151936, THREADS + 1).astype(int)
+    jobs = [(bounds[i], bounds[i + 1] - bounds[i]) for i in range(THREADS) if bounds[i + 1] > bounds[i]]
+    with ThreadPoolExecutor(THREADS) as ex:
+        res = list(ex.map(lambda j: oracle.fp8_gemv(a, codes, scales, n0=j[0], nn=j[1]), jobs))
+    y = np.concatenate([r[0] for r in res], axis=1)
+    sabs = np.concatenate([r[1] for r in res], axis=1)
+    check_logits_and_argmax(logits.cpu().numpy(), idx.cpu().numpy(), y, sabs)

@@ -1,0 +1,146 @@
+"""GPU parity of the FP8 weight variant (per-row E4M3 codes, fp8w_*) against
+the oracle.
+
+Bars: codes and row scales bit-exact; FP32 outputs within 1e-3 * S + 1e-6
+(BF16 outputs plus one BF16 ulp); argmax equal to the first maximum of the
+GPU's own logits and to the oracle's index when its top-2 gap exceeds both
+tolerances.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+TOL_REL, TOL_ABS = 1e-3, 1e-6
+
+
+def nd():
+    import nvfp4_speculative_draft_gb300 as m
+    return m
+
+
+def quantize_both(w, dev):
+    m = nd()
+    wq = m.fp8w_quantize(w.to(dev).contiguous())
+    codes, scales = oracle.fp8_quantize(workloads.bits(w))
+    torch.cuda.synchronize()
+    assert np.array_equal(wq.row_scale.cpu().numpy(), scales), "row scales differ"
+    gc = wq.codes.cpu().numpy()
+    if not np.array_equal(gc, codes):
+        bad = np.argwhere(gc != codes)[:5]
+        raise AssertionError(f"codes differ at {bad.tolist()}")
+    return wq, codes, scales
+
+
+@pytest.mark.parametrize("n,k", [(1, 32), (37, 160), (256, 512), (129, 4096)])
+def test_fp8_quantize_bit_exact(dev, n, k):
+    g = torch.Generator().manual_seed(n * 7 + k)
+    w = (torch.randn((n, k), generator=g) * 0.02 *
+         torch.exp2(torch.randint(-10, 6, (n, 1), generator=g).float())).to(torch.bfloat16)
+    quantize_both(w, dev)
+
+
+def test_fp8_quantize_zero_rows_signs_and_saturation(dev):
+    w = torch.zeros((4, 64), dtype=torch.bfloat16)
+    w[1, 3] = -0.5
+    w[1, 4] = -0.0
+    w[2] = torch.linspace(-3, 3, 64).to(torch.bfloat16)
+    w[3, 0] = 1e30
+    w[3, 1:] = torch.linspace(-1e30, 1e30, 63).to(torch.bfloat16)
+    quantize_both(w, dev)
+
+
+def test_fp8_quantize_reports_nonfinite(dev):
+    m = nd()
+    w = torch.ones((2, 64), dtype=torch.bfloat16, device=dev)
+    w[1, 5] = float("inf")
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    m.fp8w_quantize(w, dev_status=status)
+    torch.cuda.synchronize()
+    assert status.item() == 7
+
+
+@pytest.mark.parametrize("m_rows", [1, 2, 3, 8])
+def test_fp8_gemv_argmax_parity(dev, m_rows):
+    m = nd()
+    case = workloads.propose_m8(n=3001, k=640, m=m_rows)
+    wq, codes, scales = quantize_both(case.w, dev)
+    x = case.segments[0][0]
+    y, sabs = oracle.fp8_gemv(workloads.bits(x), codes, scales)
+    logits, idx = m.fp8w_gemv_argmax([(x.to(dev), None)], wq)
+    y32 = m.fp8w_gemv([(x.to(dev), None)], wq)
+    torch.cuda.synchronize()
+    lg = logits.cpu().numpy()
+    tol = TOL_REL * sabs + TOL_ABS
+    assert np.all(np.abs(lg.astype(np.float64) - y) <= tol)
+    assert np.array_equal(y32.cpu().numpy(), lg)
+    for r in range(m_rows):
+        i = int(idx[r])
+        assert i == oracle.argmax(lg[r].astype(np.float64))
+        j = oracle.argmax(y[r])
+        order = np.argsort(-y[r], kind="stable")
+        second = order[1] if order[0] == j else order[0]
+        if y[r, j] - y[r, second] > tol[r, j] + tol[r, second]:
+            assert i == j
+        else:
+            assert y[r, i] >= y[r, j] - tol[r, i] - tol[r, j]
+
+
+@pytest.mark.parametrize("m_rows", [1, 4])
+def test_fp8_gemv_two_rmsnorm_segments_bf16_out(dev, m_rows):
+    m = nd()
+    case = workloads.fc_combiner(n=300, k_seg=512, m=m_rows)
+    wq, codes, scales = quantize_both(case.w, dev)
+    (e, ge), (h, gh) = case.segments
+    out = m.fp8w_gemv([(e.to(dev), ge.to(dev), 1e-6), (h.to(dev), gh.to(dev), 1e-6)], wq,
+                      out_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    a = oracle.rmsnorm_concat([(workloads.bits(e), workloads.bits(ge), 1e-6),
+                               (workloads.bits(h), workloads.bits(gh), 1e-6)], m_rows)
+    y, sabs = oracle.fp8_gemv(a, codes, scales)
+    got = out.float().cpu().numpy().astype(np.float64)
+    assert np.all(np.abs(got - y) <= TOL_REL * sabs + TOL_ABS + np.abs(y) * 2.0 ** -8)
+
+
+def test_fp8_gathered_segment_and_prepared_activations(dev):
+    """The FP8 path takes the same activation options: a gathered embedding
+    row and, from m = 2, the once-per-call activation grid."""
+    m = nd()
+    g = torch.Generator().manual_seed(78)
+    V, H, N = 200, 256, 400
+    table = torch.randn((V, H), generator=g).to(torch.bfloat16).to(dev)
+    w = (torch.randn((N, H), generator=g) * 0.02).to(torch.bfloat16)
+    wq, codes, scales = quantize_both(w, dev)
+    idx = torch.tensor([3, 199, 0], dtype=torch.int32, device=dev)
+    gamma = (1 + 0.05 * torch.randn(H, generator=g)).to(torch.bfloat16).to(dev)
+    y_g = m.fp8w_gemv([(table, gamma, 1e-6, idx)], wq)
+    y_k = m.fp8w_gemv([(table[idx.long()].contiguous(), gamma, 1e-6)], wq, prepare=False)
+    torch.cuda.synchronize()
+    assert torch.equal(y_g, y_k)
+    a = oracle.rmsnorm_concat([(workloads.bits(table[idx.long()].cpu()), workloads.bits(gamma.cpu()),
+                                1e-6)], 3)
+    y, sabs = oracle.fp8_gemv(a, codes, scales)
+    assert np.all(np.abs(y_g.cpu().numpy().astype(np.float64) - y) <= TOL_REL * sabs + TOL_ABS)
+
+
+def test_activation_footprint_limit_is_a_shape_error(dev):
+    """m * k beyond what one CTA's shared memory holds is refused (no launch)."""
+    m = nd()
+    w = torch.zeros((32, 10240), dtype=torch.bfloat16, device=dev)
+    q8 = m.fp8w_quantize(w)
+    x = torch.zeros((8, 10240), dtype=torch.bfloat16, device=dev)
+    with pytest.raises(m.Nvfp4Error) as e:
+        m.fp8w_gemv([(x, None)], q8, prepare=False)
+    assert e.value.status == 2
+    w2 = torch.zeros((32, 16384), dtype=torch.bfloat16, device=dev)
+    q4, _ = m.nvfp4_quantize(w2)
+    x2 = torch.zeros((8, 16384), dtype=torch.bfloat16, device=dev)
+    with pytest.raises(m.Nvfp4Error) as e:
+        m.w4a16_gemv([(x2, None)], q4, prepare=False)
+    assert e.value.status == 2
+    m.w4a16_gemv([(x2[:5].contiguous(), None)], q4)  # m = 5 fits at k = 16384
+    torch.cuda.synchronize()
