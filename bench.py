@@ -10,9 +10,12 @@ ceil(4 L2 / bytes) independently quantised copies in turn: every call streams
 its weights from HBM.  The 1000 calls of a step are captured in one CUDA graph.
 
 Also reported (``detail``): the batched-propose GEMV+argmax (151936 x 5120,
-M = 1, 2, 4, 8), the fc combiner (5120 x 10240 with two RMSNorms + concat,
-M = 1, 4, 8), the prefill GEMM (2048 x 17408 x 5120, TFLOPS) and the load-time
-quantiser (17408 x 5120).
+M = 1, 2, 4, 8; M = 1, 8 also with grammar mask + top-1 log-probability), the
+FP8 weight variant of that head (M = 1, 8, and its quantiser), the chained
+propose step (fc with the embedding gathered by the previous token + LM head +
+argmax, on the device), the fc combiner (5120 x 10240 with two RMSNorms +
+concat, M = 1, 4, 8), the prefill GEMM (2048 x 17408 x 5120, TFLOPS) and the
+load-time quantiser (17408 x 5120).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
