@@ -8,7 +8,8 @@ device): ``lm_head`` (32768 x 4096, RMSNorm + GEMV + argmax, M=1), ``propose``
 concat, BF16 out, M=--m), ``gemm`` (2048 x 17408 x 5120 prefill GEMM on BF16
 operands, as the benchmark times it; ``gemm_f16`` with the FP16 staging
 workspace),
-``quantize`` (17408 x 5120).  Inputs are prepared first (their kernels run
+``quantize`` (17408 x 5120), ``propose_fp8`` / ``quantize_fp8`` (the FP8
+weight variant of the 151936 x 5120 head).  Inputs are prepared first (their kernels run
 before the measured calls, so ``ncu -k regex:<kernel> -s <n>`` can skip them),
 then the call runs --iters times and the process exits 0.
 """
@@ -28,7 +29,8 @@ def main():
     import workloads
     ap = argparse.ArgumentParser()
     ap.add_argument("--case", required=True,
-                    choices=["lm_head", "propose", "fc", "gemm", "gemm_f16", "quantize"])
+                    choices=["lm_head", "propose", "propose_fp8", "fc", "gemm", "gemm_f16", "quantize",
+                             "quantize_fp8"])
     ap.add_argument("--m", type=int, default=1)
     ap.add_argument("--iters", type=int, default=3)
     args = ap.parse_args()
@@ -50,6 +52,19 @@ def main():
         torch.cuda.empty_cache()  # keep only the quantised weight resident
         for _ in range(args.iters):
             nd.w4a16_gemv_argmax([(x, None)], wq)
+    elif args.case in ("propose_fp8", "quantize_fp8"):
+        c = workloads.propose_m8(device=dev)
+        w8 = nd.fp8w_quantize(c.w)
+        x = c.segments[0][0][:args.m].contiguous()
+        if args.case == "propose_fp8":
+            del c
+            torch.cuda.synchronize()
+            torch.cuda.empty_cache()
+        for _ in range(args.iters):
+            if args.case == "propose_fp8":
+                nd.fp8w_gemv_argmax([(x, None)], w8)
+            else:
+                nd.fp8w_quantize(c.w, out=w8)
     elif args.case == "fc":
         c = workloads.fc_combiner(device=dev)
         wq, _ = nd.nvfp4_quantize(c.w)
