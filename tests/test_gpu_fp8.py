@@ -144,3 +144,28 @@ def test_activation_footprint_limit_is_a_shape_error(dev):
     assert e.value.status == 2
     m.w4a16_gemv([(x2[:5].contiguous(), None)], q4)  # m = 5 fits at k = 16384
     torch.cuda.synchronize()
+
+
+def test_fp8_quantize_exact_midpoint_ties(dev):
+    """Rows whose scale is an exact power of two (row max 448 * 2^e) with
+    elements on E4M3 rounding midpoints (normal and subnormal) and one BF16
+    ulp either side."""
+    grid = torch.arange(0, 127, dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float64)
+    mids = ((grid[1:] + grid[:-1]) / 2)
+    mids = mids[mids.to(torch.bfloat16).double().eq(mids)]   # the midpoints BF16 holds exactly
+    assert len(mids) > 40
+    rows = []
+    for e in (-20, -4, 0, 3):
+        for sign in (1.0, -1.0):
+            r = torch.zeros(128, dtype=torch.float64)
+            r[0] = 448.0
+            r[1:1 + len(mids)] = sign * mids[:127]
+            rows.append(r * 2.0 ** e)
+    wb = torch.stack(rows).to(torch.bfloat16)
+    assert wb.double().eq(torch.stack(rows)).all()
+    bits = wb.view(torch.int16)
+    nz = (bits & 0x7FFF) != 0                              # zeros stay zeros
+    up = torch.where(nz, bits + 1, bits).view(torch.bfloat16)  # one BF16 ulp either side
+    down = torch.where(nz, bits - 1, bits).view(torch.bfloat16)
+    up[:, 0], down[:, 0] = wb[:, 0], wb[:, 0]              # keep each row's maximum
+    quantize_both(torch.cat([wb, up, down]), dev)

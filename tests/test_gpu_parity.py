@@ -349,3 +349,27 @@ def test_gemm_staged_rows_of_very_different_scales(dev):
         c = m.w4a16_gemm(a.to(dev), wq, workspace=ws)
         torch.cuda.synchronize()
         check_gemm(a, (p, s, g), c.float().cpu().numpy(), rows, cols)
+
+
+def test_quantize_exact_midpoint_ties(dev):
+    """Quotients that land exactly on E2M1 rounding midpoints (ties to even)
+    and one BF16 ulp either side: g = 2^e exactly (global max 2688 * 2^e) and
+    block scales on the E4M3 grid make every quotient exact."""
+    mids = [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0]
+    rows = []
+    for e in (-12, -3, 0):
+        for s in (448.0, 288.0, 40.0, 0.875):
+            for sign in (1.0, -1.0):
+                blk = [6.0 * s] + [sign * m * s for m in mids] + [sign * m * s for m in mids] + [0.0]
+                rows.append([v * 2.0 ** e for v in blk])
+    w = torch.tensor(rows, dtype=torch.float64)
+    wb = w.to(torch.bfloat16)
+    assert wb.double().eq(w).all()                        # the ties are exact in BF16
+    bits = wb.view(torch.int16)
+    nz = (bits & 0x7FFF) != 0                              # zeros stay zeros
+    up = torch.where(nz, bits + 1, bits).view(torch.bfloat16)  # one BF16 ulp either side
+    down = torch.where(nz, bits - 1, bits).view(torch.bfloat16)
+    up[:, 0], down[:, 0] = wb[:, 0], wb[:, 0]              # keep each block's maximum
+    blocks = torch.cat([wb, up, down, torch.zeros_like(wb)], dim=1)
+    blocks[0, 63] = 2688.0  # the global maximum: g = 2688 / 2688 = 1 exactly
+    quantize_both(blocks, dev)
