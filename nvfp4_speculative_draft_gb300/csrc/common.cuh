@@ -16,10 +16,10 @@ __device__ __forceinline__ void report(int32_t* dev_status, int32_t code) {
   if (dev_status != nullptr) atomicCAS(reinterpret_cast<int*>(dev_status), 0, code);
 }
 
-// Debug builds (-DNVFP4_DEBUG_BOUNDS) check every global and shared access of
-// the kernels against the extents its arguments imply; a failed check records
-// 1000 + tag in the caller's status word and the access is skipped.  Release
-// builds compile the checks away.
+// Debug builds (-DNVFP4_DEBUG_BOUNDS) check the GEMV's activation loads,
+// fragment stores and output stores against the extents its arguments imply;
+// a failed check records 1000 + tag in the caller's status word and the access
+// is skipped.  Release builds compile the checks away.
 #ifdef NVFP4_DEBUG_BOUNDS
 __device__ __forceinline__ bool guard(bool ok, int tag, int32_t* st) {
   if (!ok) report(st, 1000 + tag);

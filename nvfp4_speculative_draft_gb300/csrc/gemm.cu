@@ -60,7 +60,8 @@ constexpr int kEpilogueWarps = 4;
 constexpr int kThreads = (2 + kDequantWarps + kEpilogueWarps) * 32;
 // TMEM columns: two tiles' accumulators (the epilogue of one overlaps the
 // next tile's MMAs) or one tile's kMHalves accumulators
-constexpr int kTmemCols = kSingleBuf ? kMHalves * BN : 2 * kMHalves * BN;
+constexpr int pow2_at_least(int v, int p = 32) { return p >= v ? p : pow2_at_least(v, 2 * p); }
+constexpr int kTmemCols = pow2_at_least(kSingleBuf ? kMHalves * BN : 2 * kMHalves * BN);  // alloc unit
 constexpr int kPrefetch = 4;       // k steps of weight rows in flight per dequant thread
 constexpr size_t kSmemBytes = 1024 /*alignment slack*/ + (size_t)kRingBytes + 256;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
