@@ -76,7 +76,8 @@ extern "C" {
  * bytes (16-byte aligned) and m >= 2, the GEMV calls normalise the
  * activations once in a small grid of their own (one CTA per batch row) and
  * every GEMV CTA copies the result, instead of each CTA normalising all rows
- * itself; results are bit-identical either way.  Layout: the
+ * itself (both match the reference within the GEMV tolerance; the norm's
+ * sum of squares may add its partials in another order).  Layout: the
  * argmax / log-prob area above, then the per-row scale carriers at
  * W4A16_GEMV_PREP_OFFSET and the FP16 fragments 256 bytes further on. */
 #define W4A16_GEMV_PREP_OFFSET 65664

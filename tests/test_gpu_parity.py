@@ -204,7 +204,9 @@ def test_gemv_strided_activations(dev):
 @pytest.mark.parametrize("m_rows,n,k1,k2", [(2, 300, 1056, 0), (3, 1000, 512, 544), (8, 257, 2048, 1024)])
 def test_prepared_activations_match_in_kernel_prologue(dev, m_rows, n, k1, k2):
     """The once-per-call activation grid (large workspace) and the per-CTA
-    prologue (small or no workspace) give bit-identical logits and argmax."""
+    prologue (small or no workspace) both match the oracle.  (Their sums of
+    squares may add partials in different orders, so the two are compared to
+    the oracle, not to each other bit for bit.)"""
     m = nd()
     g = torch.Generator().manual_seed(n + k1 + k2)
     k = k1 + k2
@@ -224,13 +226,16 @@ def test_prepared_activations_match_in_kernel_prologue(dev, m_rows, n, k1, k2):
     y_p = m.w4a16_gemv(segs, wq, out_dtype=torch.bfloat16, workspace=big)
     y_k = m.w4a16_gemv(segs, wq, out_dtype=torch.bfloat16, prepare=False)
     torch.cuda.synchronize()
-    assert torch.equal(lg_p, lg_k) and torch.equal(idx_p, idx_k)
-    assert torch.equal(y_p.view(torch.int16), y_k.view(torch.int16))
     a = oracle.rmsnorm_concat([(workloads.bits(x.cpu()), workloads.bits(gm.cpu()), e) for x, gm, e in segs],
                               m_rows)
     y, sabs = oracle.gemv(a, wq.packed.cpu().numpy(), wq.scales.cpu().numpy(),
                           np.float32(wq.global_scale.item()))
-    check_logits(lg_p.cpu().numpy(), y, sabs)
+    for lg, idx in ((lg_p, idx_p), (lg_k, idx_k)):
+        check_logits(lg.cpu().numpy(), y, sabs)
+        check_argmax(idx.cpu().numpy(), lg.cpu().numpy(), y, sabs)
+    for yb in (y_p, y_k):
+        got = yb.float().cpu().numpy().astype(np.float64)
+        assert np.all(np.abs(got - y) <= TOL_REL * sabs + TOL_ABS + np.abs(y) * 2.0 ** -8)
 
 
 def test_argmax_ties_pick_lowest_index(dev):
