@@ -292,6 +292,11 @@ int fp8w_gemv(const w4a16_act_segment *seg, int nseg, int m, const fp8w_weight *
               int y_dtype, int64_t ldy, const nvfp4_exec *ex);
 int fp8w_gemv_argmax(const w4a16_act_segment *seg, int nseg, int m, const fp8w_weight *w,
                      float *logits, int64_t ld_logits, int32_t *argmax, const nvfp4_exec *ex);
+/* fp8w_gemv_argmax_ex -- w4a16_gemv_argmax_ex (grammar mask, top-1
+ * log-probability) with the FP8 weight. */
+int fp8w_gemv_argmax_ex(const w4a16_act_segment *seg, int nseg, int m, const fp8w_weight *w,
+                        float *logits, int64_t ld_logits, int32_t *argmax, float *logprob,
+                        const int32_t *mask, int64_t ld_mask, const nvfp4_exec *ex);
 
 #ifdef __cplusplus
 }

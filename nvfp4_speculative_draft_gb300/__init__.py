@@ -43,7 +43,7 @@ def gemv_workspace_bytes(m: int, k: int) -> int:
     return GEMV_PREP_OFFSET + 256 + (k + 255) // 256 * 512 * m
 QUANTIZE_WS_BYTES = 16
 EXPORTED = ("nvfp4_quantize", "w4a16_gemv", "w4a16_gemv_argmax", "w4a16_gemv_argmax_ex",
-            "w4a16_gemm", "fp8w_quantize", "fp8w_gemv", "fp8w_gemv_argmax")
+            "w4a16_gemm", "fp8w_quantize", "fp8w_gemv", "fp8w_gemv_argmax", "fp8w_gemv_argmax_ex")
 
 
 class Nvfp4Error(RuntimeError):
@@ -97,6 +97,8 @@ def load(path: str = LIB_PATH):
     L.fp8w_quantize.argtypes = [vp, i64, i64, vp, vp, P(_Exec)]
     L.fp8w_gemv.argtypes = [P(_Segment), i32, i32, P(_Fp8Weight), vp, i32, i64, P(_Exec)]
     L.fp8w_gemv_argmax.argtypes = [P(_Segment), i32, i32, P(_Fp8Weight), vp, i64, vp, P(_Exec)]
+    L.fp8w_gemv_argmax_ex.argtypes = [P(_Segment), i32, i32, P(_Fp8Weight), vp, i64, vp, vp, vp,
+                                      i64, P(_Exec)]
     L.w4a16_gemv_argmax_noalloc.argtypes = [P(_Segment), i32, i32, P(_Weight), vp, i64, vp, vp,
                                             vp]
     for f in EXPORTED + ("w4a16_gemv_argmax_noalloc",):
@@ -269,20 +271,11 @@ def pack_mask(allowed: torch.Tensor) -> torch.Tensor:
     return torch.where(words >= 2 ** 31, words - 2 ** 32, words).to(torch.int32)
 
 
-def w4a16_gemv_argmax_ex(segments: Sequence, weight: Nvfp4Weight, mask: Optional[torch.Tensor] = None,
-                         logprob: bool = True, logits: bool = True,
-                         out_logits: Optional[torch.Tensor] = None,
-                         out_argmax: Optional[torch.Tensor] = None,
-                         out_logprob: Optional[torch.Tensor] = None,
-                         workspace: Optional[torch.Tensor] = None, stream=None,
-                         dev_status: Optional[torch.Tensor] = None):
-    """Returns (logits FP32 [m, n] or None, argmax int32 [m], logprob FP32 [m] or None).
-
-    ``mask`` is int32 words [m, >= ceil(n/32)] (see :func:`pack_mask`) or None."""
+def _argmax_ex(call, segments, weight, n, dev, mask, logprob, logits, out_logits, out_argmax,
+               out_logprob, workspace, stream, dev_status):
     segs, m = _segments(segments)
-    dev = weight.packed.device
     if logits and out_logits is None:
-        out_logits = torch.empty((m, weight.n), dtype=torch.float32, device=dev)
+        out_logits = torch.empty((m, n), dtype=torch.float32, device=dev)
     if out_argmax is None:
         out_argmax = torch.empty(m, dtype=torch.int32, device=dev)
     if logprob and out_logprob is None:
@@ -293,15 +286,30 @@ def w4a16_gemv_argmax_ex(segments: Sequence, weight: Nvfp4Weight, mask: Optional
         raise ValueError("mask must be int32 [m, words] with unit column stride")
     ex = _exec(stream, workspace, dev_status)
     w = weight.c()
-    rc = load().w4a16_gemv_argmax_ex(segs, len(segments), m, ctypes.byref(w),
-                                     out_logits.data_ptr() if out_logits is not None else None,
-                                     out_logits.stride(0) if out_logits is not None else 0,
-                                     out_argmax.data_ptr(),
-                                     out_logprob.data_ptr() if out_logprob is not None else None,
-                                     mask.data_ptr() if mask is not None else None,
-                                     mask.stride(0) if mask is not None else 0, ctypes.byref(ex))
-    _check("w4a16_gemv_argmax_ex", rc)
+    rc = getattr(load(), call)(segs, len(segments), m, ctypes.byref(w),
+                               out_logits.data_ptr() if out_logits is not None else None,
+                               out_logits.stride(0) if out_logits is not None else 0,
+                               out_argmax.data_ptr(),
+                               out_logprob.data_ptr() if out_logprob is not None else None,
+                               mask.data_ptr() if mask is not None else None,
+                               mask.stride(0) if mask is not None else 0, ctypes.byref(ex))
+    _check(call, rc)
     return out_logits, out_argmax, out_logprob
+
+
+def w4a16_gemv_argmax_ex(segments: Sequence, weight: Nvfp4Weight, mask: Optional[torch.Tensor] = None,
+                         logprob: bool = True, logits: bool = True,
+                         out_logits: Optional[torch.Tensor] = None,
+                         out_argmax: Optional[torch.Tensor] = None,
+                         out_logprob: Optional[torch.Tensor] = None,
+                         workspace: Optional[torch.Tensor] = None, stream=None,
+                         dev_status: Optional[torch.Tensor] = None):
+    """Returns (logits FP32 [m, n] or None, argmax int32 [m], logprob FP32 [m] or None).
+
+    ``mask`` is int32 words [m, >= ceil(n/32)] (see :func:`pack_mask`) or None."""
+    return _argmax_ex("w4a16_gemv_argmax_ex", segments, weight, weight.n, weight.packed.device, mask,
+                      logprob, logits, out_logits, out_argmax, out_logprob, workspace, stream,
+                      dev_status)
 
 
 def w4a16_gemv_argmax_noalloc(segments: Sequence, weight: Nvfp4Weight,
@@ -408,3 +416,16 @@ def fp8w_gemv_argmax(segments: Sequence, weight: Fp8Weight, logits: bool = True,
                                  out_argmax.data_ptr(), ctypes.byref(ex))
     _check("fp8w_gemv_argmax", rc)
     return out_logits, out_argmax
+
+
+def fp8w_gemv_argmax_ex(segments: Sequence, weight: Fp8Weight, mask: Optional[torch.Tensor] = None,
+                        logprob: bool = True, logits: bool = True,
+                        out_logits: Optional[torch.Tensor] = None,
+                        out_argmax: Optional[torch.Tensor] = None,
+                        out_logprob: Optional[torch.Tensor] = None,
+                        workspace: Optional[torch.Tensor] = None, stream=None,
+                        dev_status: Optional[torch.Tensor] = None):
+    """:func:`w4a16_gemv_argmax_ex` with the FP8 weight."""
+    return _argmax_ex("fp8w_gemv_argmax_ex", segments, weight, weight.n, weight.codes.device, mask,
+                      logprob, logits, out_logits, out_argmax, out_logprob, workspace, stream,
+                      dev_status)

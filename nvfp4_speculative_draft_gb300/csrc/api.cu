@@ -139,6 +139,30 @@ cudaStream_t stream_of(const nvfp4_exec* ex) {
 }
 int32_t* status_of(const nvfp4_exec* ex) { return ex ? ex->dev_status : nullptr; }
 
+// Argument checks and launch shared by the two weight formats' _ex calls.
+int gemv_argmax_ex(const w4a16_act_segment* seg, int nseg, int m, const WeightRef& wr, float* logits,
+                   int64_t ld_logits, int32_t* argmax, float* logprob, const int32_t* mask,
+                   int64_t ld_mask, const nvfp4_exec* ex) {
+  const WeightRef* w = &wr;
+  int rc = check_segments(seg, nseg, m, w->k);
+  if (rc) return rc;
+  if (argmax == nullptr) return NVFP4_ERR_NULL;
+  if ((reinterpret_cast<uintptr_t>(argmax) & 3u) ||
+      (logits != nullptr && (reinterpret_cast<uintptr_t>(logits) & 3u)) ||
+      (logprob != nullptr && (reinterpret_cast<uintptr_t>(logprob) & 3u)) ||
+      (mask != nullptr && (reinterpret_cast<uintptr_t>(mask) & 3u)))
+    return NVFP4_ERR_ALIGN;
+  if (logits != nullptr && ld_logits < w->n) return NVFP4_ERR_SHAPE;
+  if (mask != nullptr && ld_mask < (w->n + 31) / 32) return NVFP4_ERR_SHAPE;
+  if (w->n > 0x7FFFFFFFLL) return NVFP4_ERR_SHAPE;
+  if (ex == nullptr || ex->workspace == nullptr || ex->workspace_bytes < W4A16_ARGMAX_EX_WS_BYTES ||
+      !aligned16(ex->workspace))
+    return NVFP4_ERR_WORKSPACE;
+  return launch_gemv(seg, nseg, m, wr, logits, NVFP4_DTYPE_F32, ld_logits, true, argmax,
+                     ex->workspace, ex->workspace_bytes, status_of(ex), stream_of(ex), logprob, mask,
+                     ld_mask);
+}
+
 }  // namespace
 
 extern "C" {
@@ -203,23 +227,15 @@ int w4a16_gemv_argmax_ex(const w4a16_act_segment* seg, int nseg, int m, const nv
                          const int32_t* mask, int64_t ld_mask, const nvfp4_exec* ex) {
   int rc = check_weight(w);
   if (rc) return rc;
-  rc = check_segments(seg, nseg, m, w->k);
+  return gemv_argmax_ex(seg, nseg, m, ref_of(w), logits, ld_logits, argmax, logprob, mask, ld_mask, ex);
+}
+
+int fp8w_gemv_argmax_ex(const w4a16_act_segment* seg, int nseg, int m, const fp8w_weight* w,
+                        float* logits, int64_t ld_logits, int32_t* argmax, float* logprob,
+                        const int32_t* mask, int64_t ld_mask, const nvfp4_exec* ex) {
+  int rc = check_fp8_weight(w);
   if (rc) return rc;
-  if (argmax == nullptr) return NVFP4_ERR_NULL;
-  if ((reinterpret_cast<uintptr_t>(argmax) & 3u) ||
-      (logits != nullptr && (reinterpret_cast<uintptr_t>(logits) & 3u)) ||
-      (logprob != nullptr && (reinterpret_cast<uintptr_t>(logprob) & 3u)) ||
-      (mask != nullptr && (reinterpret_cast<uintptr_t>(mask) & 3u)))
-    return NVFP4_ERR_ALIGN;
-  if (logits != nullptr && ld_logits < w->n) return NVFP4_ERR_SHAPE;
-  if (mask != nullptr && ld_mask < (w->n + 31) / 32) return NVFP4_ERR_SHAPE;
-  if (w->n > 0x7FFFFFFFLL) return NVFP4_ERR_SHAPE;
-  if (ex == nullptr || ex->workspace == nullptr || ex->workspace_bytes < W4A16_ARGMAX_EX_WS_BYTES ||
-      !aligned16(ex->workspace))
-    return NVFP4_ERR_WORKSPACE;
-  return launch_gemv(seg, nseg, m, ref_of(w), logits, NVFP4_DTYPE_F32, ld_logits, true, argmax,
-                     ex->workspace, ex->workspace_bytes, status_of(ex), stream_of(ex), logprob, mask,
-                     ld_mask);
+  return gemv_argmax_ex(seg, nseg, m, ref_of(w), logits, ld_logits, argmax, logprob, mask, ld_mask, ex);
 }
 
 int w4a16_gemm(const void* a_bf16, int64_t m, int64_t lda, const nvfp4_weight* w, void* c_bf16,

@@ -157,6 +157,13 @@ def test_fp8w_argument_checks(L):
     assert f(seg, 1, 1, ctypes.byref(w), 0x6000, 0, 200, ctypes.byref(ex)) == 2
     a = L.fp8w_gemv_argmax
     assert a(seg, 1, 1, ctypes.byref(w), 0x6000, 256, 0x7000, ctypes.byref(ex)) == 4
+    e = L.fp8w_gemv_argmax_ex
+    small = nd._Exec(None, 0x10000, nd.ARGMAX_WS_BYTES, None)
+    assert e(seg, 1, 1, ctypes.byref(w), 0x6000, 256, 0x7000, 0x7100, 0x7200, 16,
+             ctypes.byref(small)) == 4
+    ok = nd._Exec(None, 0x10000, nd.ARGMAX_EX_WS_BYTES, None)
+    assert e(seg, 1, 1, ctypes.byref(w), 0x6000, 256, 0x7000, 0x7100, 0x7200, 7,
+             ctypes.byref(ok)) == 2
 
 
 def test_gemm_argument_checks(L):

@@ -158,3 +158,20 @@ def test_repeat_is_bitwise_identical_and_workspace_returns_to_zero(dev):
     for _, idx, lp in outs[1:]:
         assert torch.equal(idx, outs[0][1])
         assert torch.equal(lp.view(torch.int32), outs[0][2].view(torch.int32))
+
+
+@pytest.mark.parametrize("m_rows", [1, 4])
+def test_fp8_masked_argmax_and_logprob(dev, m_rows):
+    """The same fused epilogue on the FP8 weight path."""
+    m = nd()
+    case = workloads.propose_m8(n=2600, k=384, m=m_rows)
+    codes, scales = oracle.fp8_quantize(workloads.bits(case.w))
+    wq = m.Fp8Weight(torch.from_numpy(codes).to(dev), torch.from_numpy(scales).to(dev), 2600, 384)
+    x = case.segments[0][0]
+    y, sabs = oracle.fp8_gemv(workloads.bits(x), codes, scales)
+    mask = random_mask(m_rows, 2600, 0.3, seed=200 + m_rows, pad_words=1)
+    lg, idx, lp = m.fp8w_gemv_argmax_ex([(x.to(dev), None)], wq, mask=torch.from_numpy(mask).to(dev))
+    torch.cuda.synchronize()
+    lg, idx, lp = lg.cpu().numpy(), idx.cpu().numpy(), lp.cpu().numpy()
+    for r in range(m_rows):
+        check_row(r, lg, idx, lp, y, sabs, mask)
