@@ -10,7 +10,7 @@ ceil(4 L2 / bytes) independently quantised copies in turn: every call streams
 its weights from HBM.  The 1000 calls of a step are captured in one CUDA graph.
 
 Also reported (``detail``): the batched-propose GEMV+argmax (151936 x 5120,
-M = 1, 2, 4, 8; M = 1, 8 also with grammar mask + top-1 log-probability), the
+M = 1, 2, 4, 8, 16; M = 1, 8 also with grammar mask + top-1 log-probability), the
 FP8 weight variant of that head (M = 1, 8, and its quantiser), the chained
 propose step (fc with the embedding gathered by the previous token + LM head +
 argmax, on the device), the fc combiner (5120 x 10240 with two RMSNorms +
@@ -285,13 +285,13 @@ def bench_details(dev, stream, hbm, bf16):
     import workloads
     out = {}
     # batched propose: 151936 x 5120 (437.6 MB of weights > L2)
-    case = workloads.propose_m8(device=dev)
+    case = workloads.propose_m8(m=16, device=dev)
     wq, _ = nd.nvfp4_quantize(case.w)
     case_w = case.w  # kept for the FP8 variant below
     del case.w
     x = case.segments[0][0]
     prop = {}
-    for m in (1, 2, 4, 8):
+    for m in (1, 2, 4, 8, 16):
         logits = torch.empty((m, 151936), dtype=torch.float32, device=dev)
         idx = torch.empty((m,), dtype=torch.int32, device=dev)
         xs = x[:m].contiguous()

@@ -56,22 +56,25 @@ extern "C" {
 #define NVFP4_DTYPE_F32 0
 #define NVFP4_DTYPE_BF16 1
 
-/* Largest activation batch of the GEMV calls (one MMA column per row). */
-#define W4A16_GEMV_MAX_M 8
+/* Largest activation batch of the GEMV calls: one MMA column per row, in
+ * groups of 8 columns that share each dequantised weight fragment (1..8 rows:
+ * one group; 9..16 rows: two -- the pages' batch-16 width). */
+#define W4A16_GEMV_MAX_M 16
 /* Largest total K of the GEMV calls (activations are staged on chip).  The
  * FP16 activation fragments take 2 m k bytes of one CTA's shared memory next
  * to the weight ring, so large m k combinations are refused with
  * NVFP4_ERR_SHAPE: NVFP4 weights allow m k up to about 95 000 (every m <= 5
- * at k = 16384; m = 8 up to k = 11 776), FP8 weights up to about 79 000
- * (m = 8 up to k = 9 728). */
+ * at k = 16384; m = 8 up to k = 11 776; 9..16 rows count as 16, up to
+ * k = 5 888), FP8 weights up to about 79 000 (m = 8 up to k = 9 728; 16 rows
+ * up to k = 4 864). */
 #define W4A16_GEMV_MAX_K 16384
 /* Workspace of w4a16_gemv_argmax: W4A16_GEMV_MAX_M 64-bit keys + a counter.
  * Zero it once when allocated; every completed call leaves it zeroed. */
-#define W4A16_ARGMAX_WS_BYTES 128
+#define W4A16_ARGMAX_WS_BYTES 256
 /* Most CTAs a GEMV launch uses, and the workspace of w4a16_gemv_argmax_ex
  * (keys + counter, then one (max, sum) pair per CTA and batch row). */
 #define W4A16_GEMV_MAX_CTAS 1024
-#define W4A16_ARGMAX_EX_WS_BYTES (128 + W4A16_GEMV_MAX_CTAS * 8 * 8)
+#define W4A16_ARGMAX_EX_WS_BYTES (W4A16_ARGMAX_WS_BYTES + W4A16_GEMV_MAX_CTAS * W4A16_GEMV_MAX_M * 8)
 /* Optional larger GEMV workspace: with at least W4A16_GEMV_WS_BYTES(m, k)
  * bytes (16-byte aligned) and m >= 2, the GEMV calls normalise the
  * activations once in a small grid of their own (one CTA per batch row) and
@@ -80,9 +83,10 @@ extern "C" {
  * sum of squares may add its partials in another order).  Layout: the
  * argmax / log-prob area above, then the per-row scale carriers at
  * W4A16_GEMV_PREP_OFFSET and the FP16 fragments 256 bytes further on. */
-#define W4A16_GEMV_PREP_OFFSET 65664
-#define W4A16_GEMV_WS_BYTES(m, k) \
-  ((size_t)W4A16_GEMV_PREP_OFFSET + 256 + ((size_t)(k) + 255) / 256 * 512 * (size_t)(m))
+#define W4A16_GEMV_PREP_OFFSET W4A16_ARGMAX_EX_WS_BYTES
+#define W4A16_GEMV_WS_BYTES(m, k)                                                \
+  ((size_t)W4A16_GEMV_PREP_OFFSET + 256 +                                        \
+   ((size_t)(k) + 255) / 256 * 512 * (size_t)((m) <= 8 ? (m) : W4A16_GEMV_MAX_M))
 /* Workspace of nvfp4_quantize when its absmax output is NULL. */
 #define NVFP4_QUANTIZE_WS_BYTES 16
 /* Optional workspace of w4a16_gemm that enables its FP16 staging path. */

@@ -30,17 +30,17 @@ STATUS_NAMES = {0: "OK", 1: "ERR_NULL", 2: "ERR_SHAPE", 3: "ERR_ALIGN", 4: "ERR_
                 5: "ERR_CUDA", 6: "ERR_TIMEOUT", 7: "ERR_NONFINITE", 8: "ERR_DTYPE", 9: "ERR_INDEX"}
 DTYPE_F32 = 0
 DTYPE_BF16 = 1
-GEMV_MAX_M = 8
+GEMV_MAX_M = 16
 GEMV_MAX_K = 16384
-ARGMAX_WS_BYTES = 128
+ARGMAX_WS_BYTES = 256
 GEMV_MAX_CTAS = 1024
-ARGMAX_EX_WS_BYTES = 128 + GEMV_MAX_CTAS * 8 * 8
+ARGMAX_EX_WS_BYTES = ARGMAX_WS_BYTES + GEMV_MAX_CTAS * GEMV_MAX_M * 8
 GEMV_PREP_OFFSET = ARGMAX_EX_WS_BYTES
 
 
 def gemv_workspace_bytes(m: int, k: int) -> int:
     """W4A16_GEMV_WS_BYTES: argmax / log-prob area plus prepared activations."""
-    return GEMV_PREP_OFFSET + 256 + (k + 255) // 256 * 512 * m
+    return GEMV_PREP_OFFSET + 256 + (k + 255) // 256 * 512 * (m if m <= 8 else GEMV_MAX_M)
 QUANTIZE_WS_BYTES = 16
 EXPORTED = ("nvfp4_quantize", "w4a16_gemv", "w4a16_gemv_argmax", "w4a16_gemv_argmax_ex",
             "w4a16_gemm", "fp8w_quantize", "fp8w_gemv", "fp8w_gemv_argmax", "fp8w_gemv_argmax_ex")

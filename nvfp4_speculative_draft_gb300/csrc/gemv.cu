@@ -78,7 +78,7 @@ struct GemvParams {
   unsigned int* counter;
   int32_t* argmax;
   float* logprob;            // top-1 log-probability per batch row, or null
-  float2* lse;               // per-CTA (max, sum) log-sum-exp partials [grid][8]
+  float2* lse;               // per-CTA (max, sum) log-sum-exp partials [grid][16]
   const int32_t* mask;       // grammar bitmask [m][ld_mask] int32 words, or null
   int64_t ld_mask;
   int32_t* dev_status;
@@ -187,8 +187,8 @@ __device__ __forceinline__ void e2m1_word_to_f16(uint32_t q, uint32_t& h0, uint3
 // 16-byte load covers 32t + 8w .. +7, and MMA 2w+u takes the pairs of
 // elements 4u .. 4u+3 of that word, so the MMA's column c = 2t + e + 8h is
 // element 32t + 8w + 4u + 2h + e: a B fragment is 4 consecutive activations.
-template <int BSTRIDE>
-__device__ __forceinline__ void chunk_mma(float (&acc)[4], const uint4& qg, const uint4& qh,
+template <int BSTRIDE, int NCG, int GSTRIDE>
+__device__ __forceinline__ void chunk_mma(float (&acc)[NCG][4], const uint4& qg, const uint4& qh,
                                           uint32_t sg, uint32_t sh, const uint2* bfrag) {
   uint32_t Sg[2], Sh[2];
   decode_scales(sg, Sg[0], Sg[1]);
@@ -201,12 +201,21 @@ __device__ __forceinline__ void chunk_mma(float (&acc)[4], const uint4& qg, cons
     uint32_t g0, g1, g2, g3, h0, h1, h2, h3;
     e2m1_word_to_f16(wg[w], g0, g1, g2, g3);
     e2m1_word_to_f16(wh[w], h0, h1, h2, h3);
-    const uint2 b0 = bfrag[(2 * w) * BSTRIDE];
-    mma_f16_16816(acc, f16x2_mul(g0, sG), f16x2_mul(h0, sH), f16x2_mul(g1, sG),
-                  f16x2_mul(h1, sH), b0.x, b0.y);
-    const uint2 b1 = bfrag[(2 * w + 1) * BSTRIDE];
-    mma_f16_16816(acc, f16x2_mul(g2, sG), f16x2_mul(h2, sH), f16x2_mul(g3, sG),
-                  f16x2_mul(h3, sH), b1.x, b1.y);
+    // one dequantised A fragment feeds the MMA of every column group
+    const uint32_t a0 = f16x2_mul(g0, sG), a1 = f16x2_mul(h0, sH), a2 = f16x2_mul(g1, sG),
+                   a3 = f16x2_mul(h1, sH);
+#pragma unroll
+    for (int cg = 0; cg < NCG; ++cg) {
+      const uint2 b0 = bfrag[(2 * w) * BSTRIDE + cg * GSTRIDE];
+      mma_f16_16816(acc[cg], a0, a1, a2, a3, b0.x, b0.y);
+    }
+    const uint32_t c0 = f16x2_mul(g2, sG), c1 = f16x2_mul(h2, sH), c2 = f16x2_mul(g3, sG),
+                   c3 = f16x2_mul(h3, sH);
+#pragma unroll
+    for (int cg = 0; cg < NCG; ++cg) {
+      const uint2 b1 = bfrag[(2 * w + 1) * BSTRIDE + cg * GSTRIDE];
+      mma_f16_16816(acc[cg], c0, c1, c2, c3, b1.x, b1.y);
+    }
   }
 }
 
@@ -222,8 +231,8 @@ __device__ __forceinline__ void e4m3_word_to_f16(uint32_t q, uint32_t& lo, uint3
       : "r"(q));
 }
 
-template <int BSTRIDE>
-__device__ __forceinline__ void chunk_mma_fp8(float (&acc)[4], const uint4& qg0, const uint4& qg1,
+template <int BSTRIDE, int NCG, int GSTRIDE>
+__device__ __forceinline__ void chunk_mma_fp8(float (&acc)[NCG][4], const uint4& qg0, const uint4& qg1,
                                               const uint4& qh0, const uint4& qh1,
                                               const uint2* bfrag) {
   const uint32_t wg[8] = {qg0.x, qg0.y, qg0.z, qg0.w, qg1.x, qg1.y, qg1.z, qg1.w};
@@ -233,8 +242,11 @@ __device__ __forceinline__ void chunk_mma_fp8(float (&acc)[4], const uint4& qg0,
     uint32_t g0, g1, h0, h1;
     e4m3_word_to_f16(wg[q], g0, g1);
     e4m3_word_to_f16(wh[q], h0, h1);
-    const uint2 b = bfrag[q * BSTRIDE];
-    mma_f16_16816(acc, g0, h0, g1, h1, b.x, b.y);
+#pragma unroll
+    for (int cg = 0; cg < NCG; ++cg) {
+      const uint2 b = bfrag[q * BSTRIDE + cg * GSTRIDE];
+      mma_f16_16816(acc[cg], g0, h0, g1, h1, b.x, b.y);
+    }
   }
 }
 
@@ -288,12 +300,13 @@ __device__ __forceinline__ const __nv_bfloat16* seg_row(const GemvParams& p, int
   return p.x[s] + row * p.ld[s];
 }
 
-// Shared "small" area (floats): [0,16) inverse RMS per (row, segment);
-// [16,24) per-row scale exponent carrier (BF16 magnitude bits, see
-// row_scale_pow2); [24,26) max |gamma| per segment; [32,48) max |x| per
+// Shared "small" area (floats): [0,32) inverse RMS per (row, segment);
+// [32,48) per-row scale exponent carrier (BF16 magnitude bits, see
+// row_scale_pow2); [48,50) max |gamma| per segment; [64,96) max |x| per
 // (row, segment); then per-(job, warp) partial sums of squares and maxima.
-constexpr int kSmallRowmax = 16, kSmallMaxg = 24, kSmallMaxx = 32, kSmallParts = 48;
-constexpr int kMaxJobs = 24;  // 8 rows x 2 segments + 2 gamma jobs, rounded up
+constexpr int kSmallRowmax = 32, kSmallMaxg = 48, kSmallMaxx = 64, kSmallParts = 96;
+constexpr int kMaxJobs = 40;  // 16 rows x 2 segments + 2 gamma jobs, rounded up
+constexpr int kMaxRows = 16;  // batch rows of one call (W4A16_GEMV_MAX_M)
 __host__ __device__ constexpr int small_floats(int warps) { return kSmallParts + 2 * kMaxJobs * warps; }
 
 // Kept out of line: the prologue's registers then do not compete with the
@@ -303,7 +316,8 @@ __host__ __device__ constexpr int small_floats(int warps) { return kSmallParts +
 template <int M, int WARPS>
 __device__ __noinline__ void build_fragments(const GemvParams& p, uint2* bfrag, float* small, int r0,
                                              int nrows, unsigned int* rowmax_out) {
-  constexpr int BSTRIDE = 4 * M;
+  // fragment slots per MMA k-step: column groups of (up to) 8 batch rows
+  constexpr int MC = M > 8 ? 8 : M, NCG = (M + 7) / 8, GSTRIDE = 4 * MC, BSTRIDE = GSTRIDE * NCG;
   constexpr int kWarps = WARPS, kThreads = WARPS * 32;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   float* rms = small;
@@ -428,7 +442,7 @@ __device__ __noinline__ void build_fragments(const GemvParams& p, uint2* bfrag, 
         }
       }
       const int c = kk / kChunk, t = (kk % kChunk) / 32, w = (kk % 32) / 8;
-      const int L = 4 * r + t;
+      const int L = (r / 8) * GSTRIDE + 4 * (r % 8) + t;
       if (!NVFP4_GUARD((8 * c + 2 * w + 1) * BSTRIDE + L < p.nchunks * 8 * BSTRIDE && L < BSTRIDE, 3,
                        p.dev_status))
         continue;
@@ -471,9 +485,12 @@ __device__ __forceinline__ void bar_arrive(int id, int count) {
 // time and strides over the tiles persistently.  Each warp streams its
 // (tile, chunk) items in order through its TMA ring, across tile boundaries.
 template <int M, int WARPS, bool FP8>
-__global__ void __launch_bounds__(WARPS * 32, WARPS >= 16 ? 2 : 1)
+__global__ void __launch_bounds__(WARPS * 32, (WARPS >= 16 && M <= 8) ? 2 : 1)
 gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ GemvParams p) {
-  constexpr int BSTRIDE = 4 * M;
+  // M <= 8: one MMA column per batch row.  M = 16 (any 9..16 rows): two column
+  // groups of 8 share every dequantised A fragment; MM is the call's row count.
+  constexpr int MC = M > 8 ? 8 : M, NCG = (M + 7) / 8, GSTRIDE = 4 * MC, BSTRIDE = GSTRIDE * NCG;
+  const int MM = M > 8 ? p.m : M;
   constexpr int kRing = ring_stages(M, WARPS);
   constexpr int kWarps = WARPS;
   extern __shared__ unsigned char smem_raw[];
@@ -583,13 +600,13 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
     // one bulk copy of the prepared fragments and row-scale carriers
     if (threadIdx.x == 0) {
       const uint32_t fbytes = (uint32_t)p.nchunks * 8u * BSTRIDE * 8u;
-      mbar_arrive_expect_tx(fbar, fbytes + 32u);
+      mbar_arrive_expect_tx(fbar, fbytes + 4u * kMaxRows);
       const uint32_t dst = base;  // bfrag
       for (uint32_t off = 0; off < fbytes; off += 32768u) {
         const uint32_t n = fbytes - off < 32768u ? fbytes - off : 32768u;
         bulk_copy_g2s(dst + off, reinterpret_cast<const char*>(p.frag_src) + off, n, fbar);
       }
-      bulk_copy_g2s(base + p.off_small + kSmallRowmax * 4u, p.rowmax_src, 32u, fbar);
+      bulk_copy_g2s(base + p.off_small + kSmallRowmax * 4u, p.rowmax_src, 4u * kMaxRows, fbar);
     }
     if (!mbar_wait(fbar, 0u, p.dev_status)) alive = false;
   } else {
@@ -597,25 +614,37 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
 #pragma unroll
     for (int i = 0; i < kRing; ++i)
       if (i < total) issue(i);
-    if (n_iter > 0 || blockIdx.x == 0) build_fragments<M, WARPS>(p, bfrag, rms, 0, M, nullptr);
+    if (n_iter > 0 || blockIdx.x == 0) build_fragments<M, WARPS>(p, bfrag, rms, 0, MM, nullptr);
   }
   __syncthreads();
 
   const float gsc = FP8 ? 1.0f : __ldg(p.gscale);
   // inverse activation scales of this lane's two batch columns (2t, 2t+1)
   const unsigned int* rowmax = reinterpret_cast<const unsigned int*>(rms + kSmallRowmax);
-  const float inv0 = row_scale_pow2(rowmax[min(2 * t, M - 1)], true);
-  const float inv1 = row_scale_pow2(rowmax[min(2 * t + 1, M - 1)], true);
-  const uint2* bbase = bfrag + (lane % BSTRIDE);
-  unsigned long long best[2] = {0ull, 0ull};  // running argmax keys, columns 2t and 2t+1
-  float lm[2] = {-INFINITY, -INFINITY}, ls[2] = {0.f, 0.f};  // log-sum-exp (max, sum)
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  float inv[NCG][2];  // inverse activation scales of this lane's columns 8cg + 2t + e
+#pragma unroll
+  for (int cg = 0; cg < NCG; ++cg)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) inv[cg][e] = row_scale_pow2(rowmax[min(8 * cg + 2 * t + e, MM - 1)], true);
+  const uint2* bbase = bfrag + (lane % GSTRIDE);
+  unsigned long long best[NCG][2];  // running argmax keys, columns 8cg + 2t + e
+  float lm[NCG][2], ls[NCG][2];      // log-sum-exp (max, sum)
+  float acc[NCG][4];
+#pragma unroll
+  for (int cg = 0; cg < NCG; ++cg) {
+    best[cg][0] = best[cg][1] = 0ull;
+    lm[cg][0] = lm[cg][1] = -INFINITY;
+    ls[cg][0] = ls[cg][1] = 0.f;
+    acc[cg][0] = acc[cg][1] = acc[cg][2] = acc[cg][3] = 0.f;
+  }
   int ct = 0, cc = 0;  // compute cursor
 
   // Grammar mask: the 16 rows of a tile share one 32-bit mask word per batch
   // column; the consumer warp loads the next tile's words during this tile.
   // FP8: the row scales of the consumer's rows g, g + 8, loaded the same way.
-  uint32_t mword[2] = {0xFFFFFFFFu, 0xFFFFFFFFu};
+  uint32_t mword[NCG][2];
+#pragma unroll
+  for (int cg = 0; cg < NCG; ++cg) mword[cg][0] = mword[cg][1] = 0xFFFFFFFFu;
   float rsc[2] = {0.f, 0.f};
   auto load_mask = [&](int it) {
     if (!FP8 && p.mask == nullptr) return;
@@ -627,9 +656,11 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
     }
     if (p.mask == nullptr) return;
 #pragma unroll
-    for (int e = 0; e < 2; ++e)
-      mword[e] = __ldg(reinterpret_cast<const uint32_t*>(p.mask) +
-                       min(2 * t + e, M - 1) * p.ld_mask + (tile >> 1));
+    for (int cg = 0; cg < NCG; ++cg)
+#pragma unroll
+      for (int e = 0; e < 2; ++e)
+        mword[cg][e] = __ldg(reinterpret_cast<const uint32_t*>(p.mask) +
+                             min(8 * cg + 2 * t + e, MM - 1) * p.ld_mask + (tile >> 1));
   };
   if (kpart == 0) load_mask(0);
 
@@ -637,18 +668,24 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
     const int64_t tile = ((int64_t)blockIdx.x + (int64_t)it * gridDim.x) * tpc + slot;
     if (ks > 1) {
       const int full_id = 1 + slot, empty_id = 5 + slot;  // slot < 4 when ks >= 4
-      float* mine = red + (warp * 32 + lane) * 4;
+      float* mine = red + (warp * 32 + lane) * 4 * NCG;
       if (kpart != 0) {
         // the consumer has finished tile it-1 (so no producer can arrive on the
         // full barrier twice before it completes, and the buffer is free)
         if (it >= 1) bar_sync(empty_id, ks * 32);
-        mine[0] = acc[0]; mine[1] = acc[1]; mine[2] = acc[2]; mine[3] = acc[3];
+#pragma unroll
+        for (int cg = 0; cg < NCG; ++cg)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) mine[4 * cg + i] = acc[cg][i];
         bar_arrive(full_id, ks * 32);
       } else {
         bar_sync(full_id, ks * 32);
         for (int j = 1; j < ks; ++j) {
-          const float* o = red + ((warp + j) * 32 + lane) * 4;
-          acc[0] += o[0]; acc[1] += o[1]; acc[2] += o[2]; acc[3] += o[3];
+          const float* o = red + ((warp + j) * 32 + lane) * 4 * NCG;
+#pragma unroll
+          for (int cg = 0; cg < NCG; ++cg)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) acc[cg][i] += o[4 * cg + i];
         }
         bar_arrive(empty_id, ks * 32);
       }
@@ -656,37 +693,42 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
     if (kpart == 0 && tile < p.ntiles) {
       const int64_t rows[2] = {tile * 16 + g, tile * 16 + g + 8};
 #pragma unroll
+#pragma unroll
+      for (int cg = 0; cg < NCG; ++cg) {
+#pragma unroll
       for (int h = 0; h < 2; ++h) {
         if (rows[h] >= p.n) continue;
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          const int mm = 2 * t + e;
-          if (mm >= M) continue;
-          const float v = (acc[2 * h + e] * (e ? inv1 : inv0)) * (FP8 ? rsc[h] : gsc);
+          const int mm = 8 * cg + 2 * t + e;
+          if (mm >= MM) continue;
+          const float v = (acc[cg][2 * h + e] * inv[cg][e]) * (FP8 ? rsc[h] : gsc);
           if (p.y != nullptr &&
-              NVFP4_GUARD(mm < M && rows[h] < p.n && rows[h] < p.ldy, 6, p.dev_status)) {
+              NVFP4_GUARD(mm < MM && rows[h] < p.n && rows[h] < p.ldy, 6, p.dev_status)) {
             if (p.y_dtype == NVFP4_DTYPE_F32)
               reinterpret_cast<float*>(p.y)[mm * p.ldy + rows[h]] = v;
             else
               reinterpret_cast<__nv_bfloat16*>(p.y)[mm * p.ldy + rows[h]] = __float2bfloat16_rn(v);
           }
-          if (p.keys != nullptr && ((mword[e] >> (((int)(tile & 1) << 4) + g + 8 * h)) & 1u)) {
+          if (p.keys != nullptr && ((mword[cg][e] >> (((int)(tile & 1) << 4) + g + 8 * h)) & 1u)) {
             const unsigned long long key = argmax_key(v, (uint32_t)rows[h]);
-            best[e] = key > best[e] ? key : best[e];
+            best[cg][e] = key > best[cg][e] ? key : best[cg][e];
             if (p.logprob != nullptr) {  // online log-sum-exp over the allowed logits
-              if (v > lm[e]) {
-                ls[e] = ls[e] * __expf(lm[e] - v) + 1.0f;
-                lm[e] = v;
+              if (v > lm[cg][e]) {
+                ls[cg][e] = ls[cg][e] * __expf(lm[cg][e] - v) + 1.0f;
+                lm[cg][e] = v;
               } else {
-                ls[e] += __expf(v - lm[e]);
+                ls[cg][e] += __expf(v - lm[cg][e]);
               }
             }
           }
         }
       }
+      }
     }
     if (kpart == 0) load_mask(it + 1);
-    acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+#pragma unroll
+    for (int cg = 0; cg < NCG; ++cg) acc[cg][0] = acc[cg][1] = acc[cg][2] = acc[cg][3] = 0.f;
   };
 
   for (int q0 = 0; q0 < total; q0 += kRing) {
@@ -706,7 +748,7 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
             const uint4 qg1 = *reinterpret_cast<const uint4*>(rg + 16);
             const uint4 qh0 = *reinterpret_cast<const uint4*>(rh);
             const uint4 qh1 = *reinterpret_cast<const uint4*>(rh + 16);
-            chunk_mma_fp8<BSTRIDE>(acc, qg0, qg1, qh0, qh1, bq + 8 * j * BSTRIDE);
+            chunk_mma_fp8<BSTRIDE, NCG, GSTRIDE>(acc, qg0, qg1, qh0, qh1, bq + 8 * j * BSTRIDE);
           }
         } else {
 #pragma unroll
@@ -715,7 +757,7 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
             const uint4 qh =
                 *reinterpret_cast<const uint4*>(st + (g + 8) * (64 * kItem) + j * 64 + t * 16);
             const uint32_t s2 = sreg[i][j];
-            chunk_mma<BSTRIDE>(acc, qg, qh, s2 & 0xFFFFu, s2 >> 16, bq + 8 * j * BSTRIDE);
+            chunk_mma<BSTRIDE, NCG, GSTRIDE>(acc, qg, qh, s2 & 0xFFFFu, s2 >> 16, bq + 8 * j * BSTRIDE);
           }
         }
         __syncwarp();  // every lane is done with stage i before it is refilled
@@ -735,49 +777,43 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
     bar_sync(5 + slot, ks * 32);
 
   if (p.keys == nullptr) return;
-  // lanes sharing t hold the same two batch columns: reduce over g, then per warp
+  // lanes sharing t hold the same batch columns: reduce over g, then per warp
+  float2* lred = reinterpret_cast<float2*>(kred + kWarps * kMaxRows);  // [kWarps][kMaxRows]
 #pragma unroll
-  for (int e = 0; e < 2; ++e) {
-#pragma unroll
-    for (int o = 4; o < 32; o <<= 1) {
-      const unsigned long long other = __shfl_xor_sync(0xFFFFFFFFu, best[e], o);
-      best[e] = other > best[e] ? other : best[e];
-    }
-  }
-  float2* lred = reinterpret_cast<float2*>(kred + kWarps * 8);  // [kWarps][8]
-  if (p.logprob != nullptr) {
+  for (int cg = 0; cg < NCG; ++cg) {
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
 #pragma unroll
       for (int o = 4; o < 32; o <<= 1) {
-        const float om = __shfl_xor_sync(0xFFFFFFFFu, lm[e], o);
-        const float os = __shfl_xor_sync(0xFFFFFFFFu, ls[e], o);
-        lse_merge(lm[e], ls[e], om, os);
+        const unsigned long long other = __shfl_xor_sync(0xFFFFFFFFu, best[cg][e], o);
+        best[cg][e] = other > best[cg][e] ? other : best[cg][e];
+        if (p.logprob != nullptr) {
+          const float om = __shfl_xor_sync(0xFFFFFFFFu, lm[cg][e], o);
+          const float os = __shfl_xor_sync(0xFFFFFFFFu, ls[cg][e], o);
+          lse_merge(lm[cg][e], ls[cg][e], om, os);
+        }
+      }
+      if (g == 0) {
+        kred[warp * kMaxRows + 8 * cg + 2 * t + e] = best[cg][e];
+        if (p.logprob != nullptr) lred[warp * kMaxRows + 8 * cg + 2 * t + e] = make_float2(lm[cg][e], ls[cg][e]);
       }
     }
   }
-  if (g == 0) {
-    kred[warp * 8 + 2 * t] = best[0];
-    kred[warp * 8 + 2 * t + 1] = best[1];
-    if (p.logprob != nullptr) {
-      lred[warp * 8 + 2 * t] = make_float2(lm[0], ls[0]);
-      lred[warp * 8 + 2 * t + 1] = make_float2(lm[1], ls[1]);
-    }
-  }
   __syncthreads();
-  if (threadIdx.x < (unsigned)M) {
+  if (threadIdx.x < (unsigned)MM) {
     const int m = threadIdx.x;
     unsigned long long b = 0ull;
     for (int w = 0; w < kWarps; ++w) {
-      const unsigned long long o = kred[w * 8 + m];
+      const unsigned long long o = kred[w * kMaxRows + m];
       b = o > b ? o : b;
     }
     if (b != 0ull)
       asm volatile("red.relaxed.gpu.global.max.u64 [%0], %1;" ::"l"(p.keys + m), "l"(b) : "memory");
     if (p.logprob != nullptr) {  // this CTA's log-sum-exp partial, combined in CTA order below
       float cm = -INFINITY, cs = 0.f;
-      for (int w = 0; w < kWarps; ++w) lse_merge(cm, cs, lred[w * 8 + m].x, lred[w * 8 + m].y);
-      p.lse[(int64_t)blockIdx.x * 8 + m] = make_float2(cm, cs);
+      for (int w = 0; w < kWarps; ++w)
+        lse_merge(cm, cs, lred[w * kMaxRows + m].x, lred[w * kMaxRows + m].y);
+      p.lse[(int64_t)blockIdx.x * kMaxRows + m] = make_float2(cm, cs);
     }
   }
   // Count the finished CTAs with an acquire-release add: the barrier orders this
@@ -796,13 +832,13 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
       // combine the per-CTA log-sum-exp partials: CTA b goes to thread b mod
       // blockDim, then a fixed shuffle tree and a fixed pass over the warps,
       // so the result does not depend on which CTA finished last
-      for (int m = 0; m < M; ++m) {
+      for (int m = 0; m < MM; ++m) {
         float cm = -INFINITY, cs = 0.f;
         for (unsigned int b = threadIdx.x; b < gridDim.x; b += blockDim.x) {
           float2 v;
           asm volatile("ld.relaxed.gpu.global.v2.f32 {%0, %1}, [%2];"
                        : "=f"(v.x), "=f"(v.y)
-                       : "l"(p.lse + (int64_t)b * 8 + m)
+                       : "l"(p.lse + (int64_t)b * kMaxRows + m)
                        : "memory");
           lse_merge(cm, cs, v.x, v.y);
         }
@@ -812,11 +848,11 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
           const float os = __shfl_xor_sync(0xFFFFFFFFu, cs, o);
           lse_merge(cm, cs, om, os);
         }
-        if (lane == 0) lred[warp * 8 + m] = make_float2(cm, cs);
+        if (lane == 0) lred[warp * kMaxRows + m] = make_float2(cm, cs);
       }
       __syncthreads();
     }
-    if (threadIdx.x < (unsigned)M) {
+    if (threadIdx.x < (unsigned)MM) {
       unsigned long long key;
       asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(key) : "l"(p.keys + threadIdx.x) : "memory");
       asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p.keys + threadIdx.x), "l"(0ull) : "memory");
@@ -824,7 +860,8 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
           key == 0ull ? 0 : (int32_t)(0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFull));
       if (p.logprob != nullptr) {
         float cm = -INFINITY, cs = 0.f;
-        for (int w = 0; w < kWarps; ++w) lse_merge(cm, cs, lred[w * 8 + threadIdx.x].x, lred[w * 8 + threadIdx.x].y);
+        for (int w = 0; w < kWarps; ++w)
+          lse_merge(cm, cs, lred[w * kMaxRows + threadIdx.x].x, lred[w * kMaxRows + threadIdx.x].y);
         // the winning logit back from its key (inverse of the order-preserving map)
         const uint32_t o = (uint32_t)(key >> 32);
         const float ymax = __uint_as_float((o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o);
@@ -848,7 +885,8 @@ PrepFn prep_for(int m) {
     case 5: return act_prep_kernel<5>;
     case 6: return act_prep_kernel<6>;
     case 7: return act_prep_kernel<7>;
-    default: return act_prep_kernel<8>;
+    case 8: return act_prep_kernel<8>;
+    default: return act_prep_kernel<16>;
   }
 }
 
@@ -862,7 +900,8 @@ KernelFn kernel_for(int m) {
     case 5: return gemv_kernel<5, WARPS, FP8>;
     case 6: return gemv_kernel<6, WARPS, FP8>;
     case 7: return gemv_kernel<7, WARPS, FP8>;
-    default: return gemv_kernel<8, WARPS, FP8>;
+    case 8: return gemv_kernel<8, WARPS, FP8>;
+    default: return gemv_kernel<16, WARPS, FP8>;  // 9..16 rows
   }
 }
 
@@ -874,14 +913,15 @@ struct Layout {
 Layout layout_for(int warps, int m, int nchunks, bool fp8) {
   const int kRing = ring_stages(m, warps);
   Layout l;
-  size_t off = (size_t)nchunks * 8 * 4 * m * sizeof(uint2);  // B fragments
+  const int cols = m <= 8 ? m : 16, ncg = (m + 7) / 8;        // the kernel's M, column groups
+  size_t off = (size_t)nchunks * 8 * 4 * cols * sizeof(uint2);  // B fragments
   l.off_red = (uint32_t)off;
-  off += (size_t)warps * 32 * 4 * sizeof(float);
+  off += (size_t)warps * 32 * 4 * ncg * sizeof(float);
   l.off_small = (uint32_t)off;
   off += (size_t)small_floats(warps) * sizeof(float);
   off = (off + 15) & ~(size_t)15;
   l.off_kred = (uint32_t)off;
-  off += (size_t)warps * 8 * sizeof(unsigned long long) + (size_t)warps * 8 * sizeof(float2);
+  off += (size_t)warps * kMaxRows * sizeof(unsigned long long) + (size_t)warps * kMaxRows * sizeof(float2);
   off = (off + 1023) & ~(size_t)1023;
   l.off_ring = (uint32_t)off;
   off += (size_t)warps * kRing * stage_bytes(fp8);
@@ -919,12 +959,12 @@ int launch_gemv(const w4a16_act_segment* seg, int nseg, int m, const WeightRef& 
   p.ldy = ldy;
   if (want_argmax) {
     p.keys = reinterpret_cast<unsigned long long*>(workspace);
-    p.counter = reinterpret_cast<unsigned int*>(reinterpret_cast<char*>(workspace) + 64);
+    p.counter = reinterpret_cast<unsigned int*>(reinterpret_cast<char*>(workspace) + 8 * kMaxRows);
     p.argmax = argmax;
     p.logprob = logprob;
     p.mask = mask;
     p.ld_mask = ld_mask;
-    p.lse = reinterpret_cast<float2*>(reinterpret_cast<char*>(workspace) + 128);
+    p.lse = reinterpret_cast<float2*>(reinterpret_cast<char*>(workspace) + W4A16_ARGMAX_WS_BYTES);
   }
   p.dev_status = dev_status;
   p.ntiles = nvfp4::cdiv(w.n, 16);

@@ -44,7 +44,7 @@ def main():
         for i in range(args.iters):
             nd.w4a16_gemv_argmax([(h[i:i + 1], gamma, 1e-6)], wq, logits=False)
     elif args.case == "propose":
-        c = workloads.propose_m8(device=dev)
+        c = workloads.propose_m8(m=max(8, args.m), device=dev)
         wq, _ = nd.nvfp4_quantize(c.w)
         x = c.segments[0][0][:args.m].contiguous()
         del c

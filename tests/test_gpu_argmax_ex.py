@@ -116,10 +116,11 @@ def test_logprob_unmasked(dev, m_rows):
     run(workloads.propose_m8(n=3001, k=512, m=m_rows), dev)
 
 
-@pytest.mark.parametrize("m_rows,density", [(1, 0.5), (4, 0.05), (8, 0.3)])
+@pytest.mark.parametrize("m_rows,density", [(1, 0.5), (4, 0.05), (8, 0.3), (16, 0.3)])
 def test_masked_argmax_and_logprob(dev, m_rows, density):
     case = workloads.propose_m8(n=4100, k=256, m=m_rows)
     mask = random_mask(m_rows, 4100, density, seed=100 + m_rows, pad_words=3)
+    assert case.segments[0][0].shape[0] == m_rows
     idx, _ = run(case, dev, mask=mask)
     # the mask matters: some row's unmasked winner is barred
     y, _ = oracle.gemv(workloads.bits(case.segments[0][0]), *oracle.quantize(workloads.bits(case.w))[:3])

@@ -64,7 +64,7 @@ def test_fp8_quantize_reports_nonfinite(dev):
     assert status.item() == 7
 
 
-@pytest.mark.parametrize("m_rows", [1, 2, 3, 8])
+@pytest.mark.parametrize("m_rows", [1, 2, 3, 8, 16])
 def test_fp8_gemv_argmax_parity(dev, m_rows):
     m = nd()
     case = workloads.propose_m8(n=3001, k=640, m=m_rows)

@@ -167,6 +167,27 @@ def test_gemv_small_all_batch_widths(dev, m_rows):
     run_gemv_case(workloads.propose_m8(n=1000, k=640, m=8), dev, m_rows=m_rows)
 
 
+@pytest.mark.parametrize("m_rows", [9, 12, 16])
+def test_gemv_two_column_groups(dev, m_rows):
+    """9..16 batch rows: two MMA column groups share each dequantised weight
+    fragment; logits, BF16 output and argmax against the oracle, for both
+    activation paths (once per call, per CTA)."""
+    run_gemv_case(workloads.propose_m8(n=1100, k=768, m=16), dev, m_rows=m_rows, with_bf16=True)
+    m = nd()
+    case = workloads.fc_combiner(n=300, k_seg=1024, m=16)
+    p, s, g, _ = oracle.quantize(workloads.bits(case.w))
+    wq = upload_weight(p, s, g, dev)
+    (e, ge), (h, gh) = case.segments
+    segs = [(e[:m_rows].contiguous().to(dev), ge.to(dev), 1e-6), (h[:m_rows].contiguous().to(dev), gh.to(dev), 1e-6)]
+    a = oracle.rmsnorm_concat([(workloads.bits(e[:m_rows]), workloads.bits(ge), 1e-6),
+                               (workloads.bits(h[:m_rows]), workloads.bits(gh), 1e-6)], m_rows)
+    y, sabs = oracle.gemv(a, p, s, g)
+    for prepare in (True, False):
+        out = m.w4a16_gemv(segs, wq, prepare=prepare)
+        torch.cuda.synchronize()
+        check_logits(out.cpu().numpy(), y, sabs)
+
+
 @pytest.mark.parametrize("n,k", [(16, 32), (17, 64), (100, 96), (257, 224), (2003, 1056)])
 def test_gemv_ragged_shapes(dev, n, k):
     run_gemv_case(workloads.propose_m8(n=n, k=k, m=3), dev, with_bf16=True)

@@ -57,5 +57,5 @@ def test_noalloc_rejects_batch_beyond_its_scratch(dev):
     L = nd.load()
     w = nd._Weight(0x1000, 0x2000, 0x3000, 256, 512)
     seg = (nd._Segment * 1)(nd._Segment(0x4000, 512, 512, None, 1e-6))
-    assert L.w4a16_gemv_argmax_noalloc(seg, 1, 9, ctypes.byref(w), None, 0, 0x7000, None,
+    assert L.w4a16_gemv_argmax_noalloc(seg, 1, 17, ctypes.byref(w), None, 0, 0x7000, None,
                                        None) == 2
