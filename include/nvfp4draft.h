@@ -171,7 +171,7 @@ int nvfp4_quantize(const void *w_bf16, int64_t n, int64_t k, uint8_t *packed,
  * where w~ = e4m3(s) * e2m1(c) is exact in BF16 and the sum is accumulated in
  * FP32; the global scale multiplies the finished sum.  This is the NVFP4 arm
  * of the per-precision one-row GEMV of "metrale_model_layers/layers/mtp_head.rs"
- * (MtpHead::gemv -> w4a16_decode_gemv), batched to m <= 8 rows and with the
+ * (MtpHead::gemv -> w4a16_decode_gemv), batched to m <= 16 rows and with the
  * draft head's RMSNorm + concat fused into the activation load.
  *   seg, nseg     host array of 1 or 2 segments; sum of k_seg == w->k.
  *   m             1..W4A16_GEMV_MAX_M activation rows.

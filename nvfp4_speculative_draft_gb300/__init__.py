@@ -9,7 +9,7 @@ fallback.
 The four calls keep the C names:
 
 * :func:`nvfp4_quantize`     BF16 [n, k] -> NVFP4 (packed, scales, g, absmax)
-* :func:`w4a16_gemv`         y[m, n] = g * a . w~   (m <= 8, RMSNorm/concat fused)
+* :func:`w4a16_gemv`         y[m, n] = g * a . w~   (m <= 16, RMSNorm/concat fused)
 * :func:`w4a16_gemv_argmax`  the same, FP32 logits + fused greedy argmax
 * :func:`w4a16_gemv_argmax_ex`  + grammar bitmask and top-1 log-probability
 * :func:`w4a16_gemm`         prefill C[m, n] = bf16(g * A . w~^T)
@@ -152,7 +152,7 @@ _WS = {}
 
 def argmax_workspace(device) -> torch.Tensor:
     """A zeroed GEMV workspace per device (each completed call re-zeroes its
-    argmax area), large enough for every GEMV call at any m <= 8 and k <= 16384
+    argmax area), large enough for every GEMV call at any m <= 16 and k <= 16384
     (argmax, log-probability and the once-per-call activation preparation).
     Calls on concurrent streams must pass their own workspace instead."""
     device = torch.device(device)

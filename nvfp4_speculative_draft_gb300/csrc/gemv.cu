@@ -1,4 +1,4 @@
-// gemv.cu -- batched NVFP4 W4A16 GEMV (m <= 8) with RMSNorm + concat fused on
+// gemv.cu -- batched NVFP4 W4A16 GEMV (m <= 16) with RMSNorm + concat fused on
 // the input and greedy argmax fused on the output, for sm_103a.
 //
 // What it computes (the NVFP4 GEMV of the draft head, "metrale_model_layers/
@@ -8,33 +8,40 @@
 //     y[m, n]   = g * sum_i a[m, i] * e4m3(s[n, i/16]) * e2m1(c[n, i])      (FP32)
 //     argmax[m] = lowest n with y[m, n] maximal (NaN never wins)
 //
-// Design.  The kernel is bound by streaming the packed weights (0.5625 byte per
-// weight incl. scales) from HBM.
-//   * Weight stream: every warp owns a 4-stage shared-memory ring; one lane
-//     issues a 2-D TMA copy (cp.async.bulk.tensor, 16 rows x 64 bytes = one
-//     128-element K chunk of a 16-row tile) per stage with an mbarrier
-//     completion, so 4 KB per warp are in flight without holding registers.
-//     Rows past n and bytes past k/2 arrive as zeros (TMA bounds fill), which
-//     removes every predicate from the loop.  Block scales (2 bytes per lane and
-//     row) are prefetched into registers as far ahead as the ring.
+// Design.  The kernel is bound by streaming the weights from HBM (NVFP4: 0.5625
+// byte per weight incl. scales; the FP8 variant: 1 byte + 4 per row).
+//   * Weight stream: every warp owns a 2-stage shared-memory ring; one lane
+//     issues a 2-D TMA copy (cp.async.bulk.tensor) per stage -- 16 rows x 128
+//     bytes (two 128-element K chunks of NVFP4 codes) or 16 rows x 256 bytes
+//     (two chunks of FP8 codes) -- with an mbarrier completion.  Rows past n
+//     and bytes past k arrive as zeros (TMA bounds fill), which removes every
+//     predicate from the loop.  NVFP4 block scales (2 bytes per lane and row
+//     and chunk) are prefetched into registers at issue time.
 //   * Products on the tensor cores: warp-level mma.sync m16n8k16 (FP16 in,
 //     FP32 accumulate).  A = the 16-row weight tile: each E2M1 pair becomes an
 //     exact f16x2 by the hardware conversion, times the block scale (E4M3 ->
-//     F16, exact; the product has at most 6 significant bits).  B = the (up to
-//     8) activation rows, FP16 after an exact per-row power-of-two scale that
-//     the epilogue removes.  On CUDA cores an 8-row batch would need 8 FP32
-//     FMAs per weight on top of the dequantisation; here the instruction count
-//     per weight does not depend on m.
-//   * Lane (g, t) of a warp reads rows g and g+8, K elements 32t..32t+31 of the
+//     F16, exact; the product has at most 6 significant bits); FP8 codes
+//     convert pairwise with no scale (the row scale multiplies the sum).
+//     B = the activation rows (8 MMA columns per column group; 9..16 rows use
+//     two groups that share each dequantised A fragment), FP16 after an exact
+//     per-row power-of-two scale that the epilogue removes.  On CUDA cores an
+//     8-row batch would need 8 FP32 FMAs per weight on top of the
+//     dequantisation; here the instruction count per weight does not depend
+//     on m up to 8.
+//   * Lane (g, t) of a warp reads rows g and g+8, K elements 32t..32t+31 of a
 //     chunk; MMA 2w+u takes elements 32t+8w+4u .. +3, so one B fragment is four
-//     consecutive activations, laid out once per CTA in shared memory in that
-//     order (one conflict-free 8-byte load per MMA), normalised on the way in.
-//   * Split K inside the CTA (ks warps per 16-row tile) for small n; partials
-//     are combined in a fixed order (deterministic: equal weight rows give
-//     bit-equal logits).
+//     consecutive activations, laid out in shared memory in that order (one
+//     conflict-free 8-byte load per MMA), normalised on the way in: by every
+//     CTA's prologue, or once per call by act_prep_kernel (m >= 2 with the
+//     workspace) and then copied by one bulk copy.
+//   * Split K inside the CTA (ks warps per 16-row tile) while there are fewer
+//     tile groups than resident CTAs; partials are combined in a fixed order
+//     (deterministic: equal weight rows give bit-equal logits).
 //   * Argmax: a 64-bit key (order-preserving float bits, inverted index) per
-//     row, max-reduced per lane, warp, CTA, then one atomicMax per CTA; the last
-//     CTA to finish converts the keys and returns the workspace to zero.
+//     row, max-reduced per lane, warp, CTA, then one atomic max per CTA and
+//     row; the last CTA to finish converts the keys and returns the workspace
+//     to zero.  Optional grammar mask and top-1 log-probability (an online
+//     log-sum-exp per lane, per-CTA partials combined in a fixed order).
 //   * Every mbarrier wait is bounded; one that runs out records
 //     NVFP4_ERR_TIMEOUT and the warp finishes its work without waiting again.
 #include <cuda.h>
