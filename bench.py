@@ -152,18 +152,33 @@ class EventTimer:
         return self.a.elapsed_time(self.b)
 
 
+def _reduce_device():
+    """Tensor device for collectives: the GPU under NCCL, the CPU under gloo."""
+    if torch.distributed.get_backend() == "nccl":
+        return torch.device("cuda", torch.cuda.current_device())
+    return torch.device("cpu")
+
+
 def barrier(dist_on):
     if dist_on:
         torch.distributed.barrier()
-    torch.cuda.synchronize()
+    if torch.cuda.is_available():
+        torch.cuda.synchronize()
 
 
 def max_over_ranks(v, dist_on):
+    """The slowest rank's time: every rank of a replica run uses the max."""
     if not dist_on:
         return v
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    t = torch.tensor([v], dtype=torch.float64, device=_reduce_device())
     torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
     return t.item()
+
+
+def aggregate_gbps(calls, bytes_per_call, ms_step_max, world):
+    """Whole-job throughput of N replicas (weak scaling): every rank streams
+    the same bytes per step, and the step takes the slowest rank's time."""
+    return calls * bytes_per_call / (ms_step_max * 1e-3) / 1e9 * world
 
 
 # ------------------------------------------------------------- our arm
@@ -504,10 +519,10 @@ def main():
     # stream, so the caching allocator's stream order covers all of them.
     torch.cuda.set_stream(stream)
     r = bench_lm_head(args, dev, dist_on, stream)
-    gbps = r["calls"] * r["bytes_per_call"] / (r["ms_step"] * 1e-3) / 1e9 * world
+    gbps = aggregate_gbps(r["calls"], r["bytes_per_call"], r["ms_step"], world)
     per_launch_us = r["ms_step"] * 1e3 / r["calls"]
     achieved = r["bytes_per_call"] / (per_launch_us * 1e-6) / 1e9
-    e2e_v = r["calls"] * r["bytes_per_call"] / (r["e2e_ms_step"] * 1e-3) / 1e9 * world
+    e2e_v = aggregate_gbps(r["calls"], r["bytes_per_call"], r["e2e_ms_step"], world)
     traffic = recorded_traffic("gemv_kernel_lm_head_m1")
     line = {
         "metric": METRIC, "value": gbps, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
