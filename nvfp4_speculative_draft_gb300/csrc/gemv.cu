@@ -289,8 +289,10 @@ __device__ __forceinline__ float row_scale_pow2(unsigned int maxbits, bool inver
 
 // ---------------------------------------------------------------- prologue
 // Normalise (optionally) and lay out the activations as B fragments.
-// Fragment layout: MMA index q = 8 * chunk + j, lane L = 4 * m + t (m < M):
-// uint2 at bfrag[q * 4M + L].  For the 8 activations at
+// Fragment layout: MMA index q = 8 * chunk + j; batch row m, lane quad t:
+// uint2 at bfrag[q * BSTRIDE + (m / 8) * GSTRIDE + 4 * (m % 8) + t], with
+// GSTRIDE = 4 * min(M, 8) slots per column group and BSTRIDE = GSTRIDE times
+// the number of column groups (one, or two for 9..16 rows).  For the 8 activations at
 // kk = 128 c + 32 t + 8 w (+0..7):  MMA 8c+2w gets {a0,a4},{a1,a5};
 // MMA 8c+2w+1 gets {a2,a6},{a3,a7}.  Positions past k are zero.
 // Row r of segment s: row r of x, or, for a gathered segment, table row
@@ -333,9 +335,10 @@ __device__ __noinline__ void build_fragments(const GemvParams& p, uint2* bfrag, 
   float* maxx = small + kSmallMaxx;
   float* part_ss = small + kSmallParts;                                          // [job][warp]
   unsigned int* part_mx = reinterpret_cast<unsigned int*>(part_ss + kMaxJobs * kWarps);
-  // 1. statistics.  Jobs 0 .. M*nseg-1: row r = job / nseg, segment s: sum of
-  //    squares (RMSNorm segments) and the largest |x| (BF16 magnitude bits
-  //    order like the values).  Jobs M*nseg + s: the largest |gamma_s|.  The
+  // 1. statistics.  Jobs 0 .. nrows*nseg-1: row r0 + job / nseg, segment
+  //    job % nseg: sum of squares (RMSNorm segments) and the largest |x| (BF16
+  //    magnitude bits order like the values).  Jobs nrows*nseg + s: the
+  //    largest |gamma_s|.  The
   //    CTA's warps split each job's k range; partials are combined in a fixed
   //    order, so the result does not depend on timing.
   const int JR = nrows * p.nseg, J = JR + p.nseg;
@@ -412,8 +415,8 @@ __device__ __noinline__ void build_fragments(const GemvParams& p, uint2* bfrag, 
   __syncthreads();
   // 2. normalised, scaled FP16 activations into the fragment slots.  The 8
   //    activations at kk = 128c + 32t + 8w of row m fill MMA 8c+2w (elements
-  //    0..3) and MMA 8c+2w+1 (elements 4..7) of lane 4m + t.  Positions past k
-  //    are zero.
+  //    0..3) and MMA 8c+2w+1 (elements 4..7) of slot L(m, t) above.  Positions
+  //    past k are zero.
   const int gpr = p.nchunks * (kChunk / 8);  // 8-element groups per row
   for (int r = r0; r < r0 + nrows; ++r) {
     const float sc = row_scale_pow2(rowmax[r], false);
