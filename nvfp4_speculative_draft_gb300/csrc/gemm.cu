@@ -28,8 +28,9 @@
 // (integer ops), then one packed BF16 multiply by the block scale * 2^118
 // (exact); the 2^8 left over is folded into g in the epilogue.
 // Every wait is bounded (2 s of globaltimer): a wait that runs out records
-// NVFP4_ERR_TIMEOUT in the caller's status word and the CTA unwinds, freeing
-// its TMEM.
+// NVFP4_ERR_TIMEOUT in the caller's status word and the CTA unwinds: every
+// role leaves its loop, the A loads and MMAs still in flight are waited for
+// (bounded again), and TMEM is freed.
 #include <cuda.h>
 #include <cuda_fp8.h>
 
@@ -109,6 +110,17 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
       return false;
     }
   }
+}
+// Bounded by time only: after an abort, lets work already in flight land.
+__device__ __forceinline__ bool mbar_drain(uint32_t bar, uint32_t parity, int32_t* dev_status) {
+  const unsigned long long t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer() - t0 > kWaitLimitNs) {
+      nvfp4::report(dev_status, NVFP4_ERR_TIMEOUT);
+      return false;
+    }
+  }
+  return true;
 }
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
                                             uint32_t bar) {
@@ -286,6 +298,8 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
   auto tmem_empty = [&](int b) { return bars + 8u * (kNbar + 2 + b); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kRingBytes + 8 * (kNbar + 4));
   volatile uint32_t* abort = tmem_slot + 1;
+  const uint32_t drain_bar = bars + 8u * (kNbar + 5);  // the MMAs in flight after an abort
+  static_assert(8 * (kNbar + 6) <= 256, "barriers, TMEM slot and abort flag exceed their 256 bytes");
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nk = (int)(p.k / BK);
@@ -308,6 +322,7 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
       mbar_init(tmem_full(b), 1);
       mbar_init(tmem_empty(b), kEpilogueWarps);
     }
+    mbar_init(drain_bar, 1);
     *abort = 0u;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -322,6 +337,7 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  int a_issued = 0;  // A-tile loads issued (TMA producer)
 
   if (warp == 0) {
     // ---------------------------------------------------------- TMA producer
@@ -337,6 +353,7 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
         for (int h = 0; h < kMHalves; ++h)
           tma_load_2d(a_tile(s) + (uint32_t)(h * kAHalfBytes), &tmap_a, kb * BK, (int)m0 + h * BM,
                       full_a(s));
+        a_issued = g + 1;
       }
     }
   } else if (warp == 1) {
@@ -490,6 +507,18 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
   }
   tc_fence_before();
   __syncthreads();
+  if (*abort) {
+    // A wait ran out somewhere in the CTA: the last A load on each stage and
+    // the MMAs already issued may still be in flight.  Wait for them (bounded)
+    // before TMEM is freed and the CTA's shared memory released.
+    if (warp == 0 && lane == 0)
+      for (int g = a_issued > kStagesA ? a_issued - kStagesA : 0; g < a_issued; ++g)
+        mbar_drain(full_a(g % kStagesA), (uint32_t)(g / kStagesA) & 1u, p.dev_status);
+    if (warp == 1 && lane == 0) {
+      mma_commit(drain_bar);  // arrives once every MMA this thread issued has completed
+      mbar_drain(drain_bar, 0u, p.dev_status);
+    }
+  }
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();

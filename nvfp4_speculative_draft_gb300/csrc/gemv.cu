@@ -43,7 +43,9 @@
 //     to zero.  Optional grammar mask and top-1 log-probability (an online
 //     log-sum-exp per lane, per-CTA partials combined in a fixed order).
 //   * Every mbarrier wait is bounded; one that runs out records
-//     NVFP4_ERR_TIMEOUT and the warp finishes its work without waiting again.
+//     NVFP4_ERR_TIMEOUT, the lane waits no more and issues no further copies,
+//     and before the CTA exits its copies still in flight are waited for
+//     (bounded again).
 #include <cuda.h>
 #include <cuda_fp8.h>
 
@@ -530,7 +532,10 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
   const uint32_t bars = base + p.off_bar + (uint32_t)warp * (kRing * 8);
   // chunks c with 128c + 32t < k hold this lane's data (scales past k read 0)
   const int cmax = (int)((p.k - 32 * t + kChunk - 1) / kChunk);
-  bool alive = true;  // false once a wait ran out
+  // The item whose wait ran out in this lane (kAlive while none has): from
+  // then on the lane waits no more and lane 0 issues no further copies.
+  constexpr int kAlive = 0x7FFFFFFF;
+  int failed_at = kAlive;
 
   const bool prepped = p.frag_src != nullptr;
   const uint32_t fbar = base + p.off_bar + (uint32_t)kWarps * (kRing * 8);  // fragment copy
@@ -563,7 +568,7 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
   if (total > 0) set_tile(0);
   auto issue = [&](int i) {
     const int c0 = (ib + lc) * kIt;
-    if (lane == 0) {
+    if (lane == 0 && failed_at == kAlive) {
       mbar_arrive_expect_tx(bars + 8 * i, kStage);
       tma_load_2d(ring + i * kStage, &tmap_w, (ib + lc) * kRowBytes, ltile16, bars + 8 * i);
     }
@@ -618,7 +623,7 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
       }
       bulk_copy_g2s(base + p.off_small + kSmallRowmax * 4u, p.rowmax_src, 4u * kMaxRows, fbar);
     }
-    if (!mbar_wait(fbar, 0u, p.dev_status)) alive = false;
+    if (!mbar_wait(fbar, 0u, p.dev_status)) failed_at = 0;
   } else {
     // start streaming before the activation prologue
 #pragma unroll
@@ -703,37 +708,36 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
     if (kpart == 0 && tile < p.ntiles) {
       const int64_t rows[2] = {tile * 16 + g, tile * 16 + g + 8};
 #pragma unroll
-#pragma unroll
       for (int cg = 0; cg < NCG; ++cg) {
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        if (rows[h] >= p.n) continue;
+        for (int h = 0; h < 2; ++h) {
+          if (rows[h] >= p.n) continue;
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int mm = 8 * cg + 2 * t + e;
-          if (mm >= MM) continue;
-          const float v = (acc[cg][2 * h + e] * inv[cg][e]) * (FP8 ? rsc[h] : gsc);
-          if (p.y != nullptr &&
-              NVFP4_GUARD(mm < MM && rows[h] < p.n && rows[h] < p.ldy, 6, p.dev_status)) {
-            if (p.y_dtype == NVFP4_DTYPE_F32)
-              reinterpret_cast<float*>(p.y)[mm * p.ldy + rows[h]] = v;
-            else
-              reinterpret_cast<__nv_bfloat16*>(p.y)[mm * p.ldy + rows[h]] = __float2bfloat16_rn(v);
-          }
-          if (p.keys != nullptr && ((mword[cg][e] >> (((int)(tile & 1) << 4) + g + 8 * h)) & 1u)) {
-            const unsigned long long key = argmax_key(v, (uint32_t)rows[h]);
-            best[cg][e] = key > best[cg][e] ? key : best[cg][e];
-            if (p.logprob != nullptr) {  // online log-sum-exp over the allowed logits
-              if (v > lm[cg][e]) {
-                ls[cg][e] = ls[cg][e] * __expf(lm[cg][e] - v) + 1.0f;
-                lm[cg][e] = v;
-              } else {
-                ls[cg][e] += __expf(v - lm[cg][e]);
+          for (int e = 0; e < 2; ++e) {
+            const int mm = 8 * cg + 2 * t + e;
+            if (mm >= MM) continue;
+            const float v = (acc[cg][2 * h + e] * inv[cg][e]) * (FP8 ? rsc[h] : gsc);
+            if (p.y != nullptr &&
+                NVFP4_GUARD(mm < MM && rows[h] < p.n && rows[h] < p.ldy, 6, p.dev_status)) {
+              if (p.y_dtype == NVFP4_DTYPE_F32)
+                reinterpret_cast<float*>(p.y)[mm * p.ldy + rows[h]] = v;
+              else
+                reinterpret_cast<__nv_bfloat16*>(p.y)[mm * p.ldy + rows[h]] = __float2bfloat16_rn(v);
+            }
+            if (p.keys != nullptr && ((mword[cg][e] >> (((int)(tile & 1) << 4) + g + 8 * h)) & 1u)) {
+              const unsigned long long key = argmax_key(v, (uint32_t)rows[h]);
+              best[cg][e] = key > best[cg][e] ? key : best[cg][e];
+              if (p.logprob != nullptr) {  // online log-sum-exp over the allowed logits
+                if (v > lm[cg][e]) {
+                  ls[cg][e] = ls[cg][e] * __expf(lm[cg][e] - v) + 1.0f;
+                  lm[cg][e] = v;
+                } else {
+                  ls[cg][e] += __expf(v - lm[cg][e]);
+                }
               }
             }
           }
         }
-      }
       }
     }
     if (kpart == 0) load_mask(it + 1);
@@ -746,7 +750,8 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
     for (int i = 0; i < kRing; ++i) {
       const int q = q0 + i;
       if (q < total) {
-        if (alive) alive = mbar_wait(bars + 8 * i, (uint32_t)(q / kRing) & 1u, p.dev_status);
+        if (failed_at == kAlive && !mbar_wait(bars + 8 * i, (uint32_t)(q / kRing) & 1u, p.dev_status))
+          failed_at = q;
         const unsigned char* st = smem + (ring - base) + i * kStage;
         const uint2* bq = bbase + (int64_t)(8 * kIt * (ib + cc)) * BSTRIDE;
         if constexpr (FP8) {  // box rows are two 128-element chunks of codes
@@ -785,6 +790,15 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
 
   if (ks > 1 && kpart != 0 && n_iter > 0)  // match the consumer's last "empty" arrival
     bar_sync(5 + slot, ks * 32);
+  // After a wait ran out in lane 0, the copies of items failed_at ..
+  // failed_at + kRing - 1 (the last one on each ring stage) may still be in
+  // flight, and thread 0's fragment copy too: wait for them, again bounded,
+  // before the CTA's shared memory can be released.
+  if (lane == 0 && failed_at != kAlive) {
+    for (int q = failed_at; q < total && q < failed_at + kRing; ++q)
+      mbar_wait(bars + 8 * (q % kRing), (uint32_t)(q / kRing) & 1u, p.dev_status);
+    if (threadIdx.x == 0 && prepped) mbar_wait(fbar, 0u, p.dev_status);
+  }
 
   if (p.keys == nullptr) return;
   // lanes sharing t hold the same batch columns: reduce over g, then per warp

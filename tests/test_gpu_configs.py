@@ -117,9 +117,11 @@ def test_lm_head_config_full(dev):
     g = check_gpu_quant(wq, amax, wb)
     h, gamma = case.segments[0]
     pk, sc = wq.packed.cpu().numpy(), wq.scales.cpu().numpy()
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
     for r in range(3):
-        logits, idx = m.w4a16_gemv_argmax([(h[r:r + 1], gamma, 1e-6)], wq)
+        logits, idx = m.w4a16_gemv_argmax([(h[r:r + 1], gamma, 1e-6)], wq, dev_status=status)
         torch.cuda.synchronize()
+        assert status.item() == 0  # no bounded wait ran out, no index reported
         a = oracle.rmsnorm_concat([(workloads.bits(h[r:r + 1]), workloads.bits(gamma), 1e-6)], 1)
         y, sabs = par_gemv(a, pk, sc, g)
         check_logits_and_argmax(logits.cpu().numpy(), idx.cpu().numpy(), y, sabs)
@@ -185,9 +187,11 @@ def test_fc_combiner_config_full(dev, mm):
     wq, amax = m.nvfp4_quantize(case.w)
     g = float(wq.global_scale.item())
     (e, ge), (h, gh) = case.segments
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
     out = m.w4a16_gemv([(e[:mm].contiguous(), ge, 1e-6), (h[:mm].contiguous(), gh, 1e-6)], wq,
-                       out_dtype=torch.bfloat16)
+                       out_dtype=torch.bfloat16, dev_status=status)
     torch.cuda.synchronize()
+    assert status.item() == 0
     a = oracle.rmsnorm_concat([(workloads.bits(e[:mm]), workloads.bits(ge), 1e-6),
                                (workloads.bits(h[:mm]), workloads.bits(gh), 1e-6)], mm)
     y, sabs = par_gemv(a, wq.packed.cpu().numpy(), wq.scales.cpu().numpy(), np.float32(g))
@@ -204,9 +208,11 @@ def test_prefill_gemm_config_sampled(dev):
     wb = workloads.bits(case.w)
     g = check_gpu_quant(wq, amax, wb)
     ws = torch.empty(m.gemm_workspace_bytes(2048, 5120), dtype=torch.uint8, device=dev)
-    c = m.w4a16_gemm(case.a, wq, workspace=ws)   # FP16 staging path
-    c_bf16 = m.w4a16_gemm(case.a, wq)            # the launch the benchmark times
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    c = m.w4a16_gemm(case.a, wq, workspace=ws, dev_status=status)  # FP16 staging path
+    c_bf16 = m.w4a16_gemm(case.a, wq, dev_status=status)            # the launch the benchmark times
     torch.cuda.synchronize()
+    assert status.item() == 0  # no bounded wait ran out
     rng = np.random.default_rng(12)
     rows = np.concatenate([rng.integers(0, 2048, 8192), np.full(17408, 5), np.full(17408, 2047),
                            np.arange(2048), np.arange(2048)])
