@@ -36,11 +36,17 @@ _i64p = ctypes.POINTER(ctypes.c_int64)
 _i64 = ctypes.c_int64
 
 
+# A different build of the oracle to load instead of the in-tree one: the
+# mutation test points this at deliberately broken copies of the C source to
+# check that the pins in tests/test_oracle.py catch each mistake.
+LIB_OVERRIDE_ENV = "NVFP4_ORACLE_LIB"
+
+
 def lib():
     """Build (if needed) and load the oracle's shared library."""
     global _LIB
     if _LIB is None:
-        path = _build.build()
+        path = os.environ.get(LIB_OVERRIDE_ENV) or _build.build()
         L = ctypes.CDLL(path)
         L.oracle_e2m1_value.argtypes = [ctypes.c_int]
         L.oracle_e2m1_value.restype = ctypes.c_double

@@ -22,11 +22,16 @@ def build(force: bool = False) -> str:
             and os.path.getmtime(LIB) >= os.path.getmtime(SRC)):
         return LIB
     tmp = LIB + f".tmp{os.getpid()}"
-    cmd = ["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math",
-           "-fPIC", "-shared", "-Wall", "-Wextra", "-o", tmp, SRC, "-lm"]
-    subprocess.run(cmd, check=True)
+    compile_source(SRC, tmp)
     os.replace(tmp, LIB)
     return LIB
+
+
+def compile_source(src: str, out: str) -> None:
+    """gcc with the oracle's flags: `src` (a C file) -> shared library `out`."""
+    cmd = ["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math",
+           "-fPIC", "-shared", "-Wall", "-Wextra", "-o", out, src, "-lm"]
+    subprocess.run(cmd, check=True)
 
 
 if __name__ == "__main__":

@@ -212,6 +212,20 @@ def test_quantize_all_zero_tensor_and_blocks():
     assert not packed[1].any() and not packed[0, :8].any()
 
 
+def test_global_absmax_against_numpy():
+    """The largest magnitude, whatever its sign: each matrix has one planted
+    extreme, negative or positive, at a random position."""
+    rng = np.random.default_rng(8)
+    for trial in range(6):
+        x = rng.standard_normal((17, 48)) * 0.02
+        r, c = rng.integers(0, 17), rng.integers(0, 48)
+        x[r, c] = (-1.0 if trial % 2 == 0 else 1.0) * 0.5
+        wb = workloads.bits(torch.from_numpy(x).to(torch.bfloat16))
+        xf = oracle.bf16_bits_to_f32(wb)
+        assert oracle.global_absmax(wb) == np.abs(xf).max() == np.float32(0.5)
+        assert oracle.quantize(wb)[3] == np.float32(0.5)
+
+
 def test_quantize_sign_symmetry():
     case = workloads.tiny(n=32, k=128)
     wb = workloads.bits(case.w)
@@ -269,6 +283,11 @@ def test_rmsnorm_textbook_and_constant_rows():
     out = oracle.rmsnorm_concat([(workloads.bits(c), workloads.bits(gamma), 1e-6)], 1)
     ref = -gd / np.sqrt(1 + 1e-6 / 0.5625)
     assert np.array_equal(out[0], oracle.bf16_round(ref))
+    # A row small enough that eps is not negligible: c = 2^-10, c^2 ~ eps.
+    c2 = torch.full((1, ks), 2.0 ** -10).to(torch.bfloat16)
+    out2 = oracle.rmsnorm_concat([(workloads.bits(c2), workloads.bits(gamma), 1e-6)], 1)
+    ref2 = gd / np.sqrt(1 + 1e-6 / 2.0 ** -20)
+    assert np.array_equal(out2[0], oracle.bf16_round(ref2))
     # No gamma: copy; segments concatenated in argument order.
     out = oracle.rmsnorm_concat([(workloads.bits(x), None, 0.0),
                                  (workloads.bits(c.expand(m, ks)), workloads.bits(gamma), 1e-6)], m)
@@ -447,10 +466,12 @@ def test_fp8_codes_match_torch_rne_of_binary32_quotients():
 def test_fp8_zero_row_and_signs():
     w = torch.zeros((3, 32), dtype=torch.bfloat16)
     w[1, 3] = -0.5
+    w[1, 5] = -0.0                                 # the code keeps the sign of x
     w[2] = torch.linspace(-1, 1, 32).to(torch.bfloat16)
     codes, scales = oracle.fp8_quantize(workloads.bits(w))
     assert scales[0] == 0.0 and not codes[0].any()
     assert codes[1, 3] == 0xFE and scales[1] == np.float32(0.5) / np.float32(448.0)
+    assert codes[1, 5] == 0x80 and codes[1, 4] == 0x00
     neg, pos = codes[2, :16], codes[2, 16:][::-1]
     assert np.array_equal(neg & 0x7F, pos & 0x7F) and np.all(neg & 0x80) and not np.any(pos & 0x80)
 
