@@ -47,7 +47,9 @@ extern "C" {
 #define NVFP4_ERR_ALIGN 3      /* a pointer or leading dimension misaligned  */
 #define NVFP4_ERR_WORKSPACE 4  /* workspace missing, too small or misaligned */
 #define NVFP4_ERR_CUDA 5       /* a kernel launch failed                     */
-#define NVFP4_ERR_TIMEOUT 6    /* device: a bounded wait gave up             */
+#define NVFP4_ERR_TIMEOUT 6    /* device: a bounded wait gave up; the call's
+                                  outputs are not valid (a GEMV still returns
+                                  its argmax workspace to zero)             */
 #define NVFP4_ERR_NONFINITE 7  /* device: Inf/NaN in the quantiser's input   */
 #define NVFP4_ERR_DTYPE 8      /* unknown output dtype                       */
 #define NVFP4_ERR_INDEX 9      /* device: a gather index out of range; row 0 */
@@ -216,8 +218,9 @@ int w4a16_gemv_argmax(const w4a16_act_segment *seg, int nseg, int m,
  *             mtp_head.rs" (MtpHead fields) writes per row, and what the draft
  *             confidence stop there reads (last_conf_bits).  FP32 exp/log; the
  *             per-CTA partials are combined in a fixed order.
- * Workspace: W4A16_ARGMAX_EX_WS_BYTES, 16-byte aligned, zeroed once when
- * allocated (each completed call re-zeroes its first 128 bytes).
+ * Workspace: W4A16_ARGMAX_EX_WS_BYTES, 16-byte aligned, its first
+ * W4A16_ARGMAX_WS_BYTES zeroed once when allocated (each completed call
+ * returns them to zero); the rest is scratch that every call overwrites.
  */
 int w4a16_gemv_argmax_ex(const w4a16_act_segment *seg, int nseg, int m, const nvfp4_weight *w,
                          float *logits, int64_t ld_logits, int32_t *argmax, float *logprob,

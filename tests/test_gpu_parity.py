@@ -130,6 +130,7 @@ def test_quantize_special_values(dev):
     x[5, 7] = 300.0                                        # dominant element: most scales tiny
     w = torch.from_numpy(x).to(torch.bfloat16)
     w.view(torch.int16)[1] = -32768                        # exact -0.0 bit pattern
+    w.view(torch.int16)[6, 3] = -32768                     # -0.0 inside a non-zero block: code 0x8
     quantize_both(w, dev)
     quantize_both(torch.zeros((8, 64), dtype=torch.bfloat16), dev)
     big = torch.full((4, 32), 3.3e38).to(torch.bfloat16)
