@@ -65,10 +65,10 @@ extern "C" {
 /* Largest total K of the GEMV calls (activations are staged on chip).  The
  * FP16 activation fragments take 2 m k bytes of one CTA's shared memory next
  * to the weight ring, so large m k combinations are refused with
- * NVFP4_ERR_SHAPE: NVFP4 weights allow m k up to about 95 000 (every m <= 5
- * at k = 16384; m = 8 up to k = 11 776; 9..16 rows count as 16, up to
- * k = 5 888), FP8 weights up to about 79 000 (m = 8 up to k = 9 728; 16 rows
- * up to k = 4 864). */
+ * NVFP4_ERR_SHAPE.  Largest k per batch width (9..16 rows count as 16):
+ *   NVFP4 weights: m <= 5: 16384; m = 6: 15 616; 7: 13 312; 8: 11 776; 16: 5 632
+ *   FP8 weights:   m <= 4: 16384; m = 5: 15 360; 6: 12 800; 7: 11 008; 8: 9 728;
+ *                  16: 4 608 */
 #define W4A16_GEMV_MAX_K 16384
 /* Workspace of w4a16_gemv_argmax: W4A16_GEMV_MAX_M 64-bit keys + a counter.
  * Zero it once when allocated; every completed call leaves it zeroed. */

@@ -128,6 +128,12 @@ def test_fp8_gathered_segment_and_prepared_activations(dev):
     assert np.all(np.abs(y_g.cpu().numpy().astype(np.float64) - y) <= TOL_REL * sabs + TOL_ABS)
 
 
+@pytest.mark.parametrize("m_rows,k_max", [(4, 16384), (8, 9728), (16, 4608)])
+def test_fp8_gemv_at_the_activation_size_limit(dev, m_rows, k_max):
+    from test_gpu_parity import run_at_size_limit
+    run_at_size_limit(dev, m_rows, k_max, fp8=True)
+
+
 def test_activation_footprint_limit_is_a_shape_error(dev):
     """m * k beyond what one CTA's shared memory holds is refused (no launch)."""
     m = nd()

@@ -189,6 +189,48 @@ def test_gemv_two_column_groups(dev, m_rows):
         check_logits(out.cpu().numpy(), y, sabs)
 
 
+def run_at_size_limit(dev, m_rows, k_max, fp8):
+    """RMSNorm + GEMV + argmax at the largest k one batch width can stage
+    (the limits listed in the header), through both activation paths, on a
+    ragged number of weight rows; then the refusal 32 columns past it."""
+    m = nd()
+    g = torch.Generator().manual_seed(m_rows * 100000 + k_max)
+    n = 70
+    w = (torch.randn((n, k_max), generator=g) * 0.02).to(torch.bfloat16)
+    x = torch.randn((m_rows, k_max), generator=g).to(torch.bfloat16)
+    gamma = (1 + 0.05 * torch.randn(k_max, generator=g)).to(torch.bfloat16)
+    a = oracle.rmsnorm_concat([(workloads.bits(x), workloads.bits(gamma), 1e-6)], m_rows)
+    if fp8:
+        codes, scales = oracle.fp8_quantize(workloads.bits(w))
+        wq = m.Fp8Weight(torch.from_numpy(codes).to(dev), torch.from_numpy(scales).to(dev), n, k_max)
+        y, sabs = oracle.fp8_gemv(a, codes, scales)
+        gemv, gemv_argmax, quantize = m.fp8w_gemv, m.fp8w_gemv_argmax, m.fp8w_quantize
+    else:
+        p, s, gs, _ = oracle.quantize(workloads.bits(w))
+        wq = upload_weight(p, s, gs, dev)
+        y, sabs = oracle.gemv(a, p, s, gs)
+        gemv, gemv_argmax = m.w4a16_gemv, m.w4a16_gemv_argmax
+        quantize = lambda t: m.nvfp4_quantize(t)[0]  # noqa: E731
+    segs = [(x.to(dev), gamma.to(dev), 1e-6)]
+    logits, idx = gemv_argmax(segs, wq)                  # once-per-call preparation (m >= 2)
+    y_cta = gemv(segs, wq, prepare=False)                 # every CTA normalises itself
+    torch.cuda.synchronize()
+    lg = logits.cpu().numpy()
+    check_logits(lg, y, sabs)
+    check_logits(y_cta.cpu().numpy(), y, sabs)
+    check_argmax(idx.cpu().numpy(), lg, y, sabs)
+    w2 = quantize(torch.zeros((32, k_max + 32), dtype=torch.bfloat16, device=dev))
+    x2 = torch.zeros((m_rows, k_max + 32), dtype=torch.bfloat16, device=dev)
+    with pytest.raises(m.Nvfp4Error) as e:
+        gemv([(x2, None)], w2, prepare=False)
+    assert e.value.status == 2  # NVFP4_ERR_SHAPE
+
+
+@pytest.mark.parametrize("m_rows,k_max", [(5, 16384), (8, 11776), (16, 5632)])
+def test_gemv_at_the_activation_size_limit(dev, m_rows, k_max):
+    run_at_size_limit(dev, m_rows, k_max, fp8=False)
+
+
 @pytest.mark.parametrize("n,k", [(16, 32), (17, 64), (100, 96), (257, 224), (2003, 1056)])
 def test_gemv_ragged_shapes(dev, n, k):
     run_gemv_case(workloads.propose_m8(n=n, k=k, m=3), dev, with_bf16=True)
