@@ -30,6 +30,7 @@ import subprocess
 import sys
 import threading
 import time
+from concurrent.futures import ThreadPoolExecutor
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
@@ -38,6 +39,10 @@ import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
 METRIC = "NVFP4 W4A16 draft-head GEMV+argmax HBM GB/s; M=128 prefill GEMM TFLOPS"
+# Nominal GB300 rates the fractions are also quoted against, next to the
+# measured ones: HBM3e 8 TB/s, dense BF16 2.25 PFLOP/s.
+NOMINAL_HBM_GBS = 8000.0
+NOMINAL_BF16_TFLOPS = 2250.0
 WORKLOAD = "draft LM-head RMSNorm+GEMV+argmax, N=32768 K=4096 M=1, 1000 seeded rows per step"
 
 
@@ -48,6 +53,51 @@ def peaks():
         return d["hbm_gbs"], d["bf16_tflops"], d.get("bf16_tflops_sustained"), "measured"
     except Exception:
         return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def add_nominal_fractions(detail, bf16_sustained=None):
+    """Next to each measured-peak fraction of `detail` (nested dicts), the
+    fraction of the nominal rate, and for TFLOPS also of the measured
+    sustained BF16 rate."""
+    for v in detail.values():
+        if not isinstance(v, dict):
+            continue
+        if "GBps" in v:
+            v["frac_of_nominal_8000"] = v["GBps"] / NOMINAL_HBM_GBS
+        if "TFLOPS" in v:
+            v["frac_of_nominal_bf16"] = v["TFLOPS"] / NOMINAL_BF16_TFLOPS
+            if bf16_sustained:
+                v["frac_of_measured_bf16_sustained"] = v["TFLOPS"] / bf16_sustained
+        add_nominal_fractions(v, bf16_sustained)
+
+
+def split_rows(n, parts):
+    """[(n0, nn), ...]: `parts` contiguous, non-empty ranges covering rows 0..n-1."""
+    bounds = [n * j // parts for j in range(parts + 1)]
+    return [(bounds[j], bounds[j + 1] - bounds[j]) for j in range(parts) if bounds[j + 1] > bounds[j]]
+
+
+def host_cpu():
+    """Model and logical core count of the host CPU (lscpu, else /proc/cpuinfo)."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except Exception:
+        pass
+    if model is None:
+        try:
+            with open("/proc/cpuinfo") as f:
+                for line in f:
+                    if line.lower().startswith("model name"):
+                        model = line.split(":", 1)[1].strip()
+                        break
+        except OSError:
+            pass
+    return {"model": model, "nproc": os.cpu_count()}
 
 
 # ------------------------------------------------------------------ clocks
@@ -442,12 +492,34 @@ class OracleLmHead:
             o.argmax(y[0])
         return (time.perf_counter() - t0) / rows
 
+    def time_rows_all_cores(self, rows, threads):
+        """The same per-row work with the oracle's GEMV run on `threads`
+        contiguous row ranges of the head at once (ctypes releases the GIL);
+        the oracle's code is unchanged."""
+        o = self.oracle
+        ranges = split_rows(self.p.shape[0], threads)
+        t0 = time.perf_counter()
+        with ThreadPoolExecutor(threads) as ex:
+            for r in range(rows):
+                a = o.rmsnorm_concat([(self.hb[r % 8:r % 8 + 1], self.gb, 1e-6)], 1)
+                parts = list(ex.map(lambda j: o.gemv(a, self.p, self.s, self.g, n0=j[0], nn=j[1])[0],
+                                    ranges))
+                o.argmax(np.concatenate(parts, axis=1)[0])
+        return (time.perf_counter() - t0) / rows
+
     def baseline(self, rows=2):
         dt = self.time_rows(rows)
+        threads = os.cpu_count() or 1
+        dt_all = self.time_rows_all_cores(rows, threads)
         return {"value": self.per_call / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
                 "sample": f"{rows} of the 1000 hidden rows of a step (RMSNorm + GEMV + argmax "
                           "over the full 32768x4096 head each), one thread; GB/s scaled from "
-                          "the per-row time", "s_per_call": dt}
+                          "the per-row time", "s_per_call": dt,
+                "all_cores": {"value": self.per_call / dt_all / 1e9, "unit": "GB/s",
+                              "cores": threads,
+                              "sample": f"the same {rows} rows, the oracle's GEMV split over "
+                                        f"{threads} threads by weight rows"},
+                "host": host_cpu()}
 
 
 def run_reference(args):
@@ -463,7 +535,7 @@ def run_reference(args):
     cb = {"value": v, "unit": "GB/s", "cores": 1, "kind": "oracle",
           "sample": "each step is 1 of the 1000 hidden rows of a step of the GPU arm "
                     "(RMSNorm + GEMV + argmax over the full 32768x4096 head), one thread; "
-                    "GB/s scaled from the per-row time"}
+                    "GB/s scaled from the per-row time", "host": host_cpu()}
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": dt * 1e3 * 1000, "higher_is_better": True,
@@ -534,6 +606,7 @@ def main():
                    "parallelism": "replicas" if world > 1 else "single"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": achieved / hbm, "traffic": traffic, "peak_source": src,
+                     "nominal_peak": NOMINAL_HBM_GBS, "frac_of_nominal": achieved / NOMINAL_HBM_GBS,
                      "kernel": "gemv_kernel", "per_launch_us": per_launch_us,
                      "per_launch_note": "graph-replayed step time / calls (events on the "
                                         "launching stream); one gemv_kernel launch per call",
@@ -545,6 +618,7 @@ def main():
     }
     if not args.no_detail and rank == 0:
         line["detail"] = bench_details(dev, stream, hbm, bf16)
+        add_nominal_fractions(line["detail"], bf16_sus)
     if rank == 0 and not args.no_cpu_baseline:
         cb = OracleLmHead().baseline()
         cb.pop("s_per_call", None)
