@@ -109,6 +109,25 @@ class OracleError(RuntimeError):
     pass
 
 
+def _need(cond, msg):
+    """Argument check before a call into C (which trusts its sizes)."""
+    if not cond:
+        raise ValueError(msg)
+
+
+def _check_weight(packed, scales, k=None):
+    """packed [n, k/2] and scales [n, k/16] of one weight (k given or implied)."""
+    _need(packed.ndim == 2 and scales.ndim == 2, "packed and scales must be 2-D")
+    n, kh = packed.shape
+    _need(k is None or kh * 2 == k, f"packed has {kh * 2} columns of codes, activations {k}")
+    _need((kh * 2) % 16 == 0 and scales.shape == (n, kh * 2 // 16),
+          f"scales must be [{n}, {kh * 2 // 16}], got {list(scales.shape)}")
+
+
+def _check_range(n0, nn, n):
+    _need(0 <= n0 and 0 <= nn and n0 + nn <= n, f"rows [{n0}, {n0 + nn}) outside [0, {n})")
+
+
 # ----------------------------------------------------------------- format
 
 def e2m1_value(code: int) -> float:
@@ -179,8 +198,10 @@ def quantize(w_bits):
 def quantize_rows(w_bits, rows, g):
     """Quantise selected rows of w[n, k] with a given global scale g."""
     w = _c(w_bits, np.uint16)
+    _need(w.ndim == 2, "w must be 2-D")
     n, k = w.shape
-    rows = np.asarray(rows, dtype=np.int64)
+    rows = np.asarray(rows, dtype=np.int64).ravel()
+    _need(np.all((rows >= 0) & (rows < n)), "row index outside the weight")
     packed = np.empty((len(rows), k // 2), dtype=np.uint8)
     scales = np.empty((len(rows), k // 16), dtype=np.uint8)
     for j, r in enumerate(rows):
@@ -194,10 +215,12 @@ def quantize_rows(w_bits, rows, g):
 def dequant(packed, scales, g, row0=0, nrows=None) -> np.ndarray:
     packed = _c(packed, np.uint8)
     scales = _c(scales, np.uint8)
+    _check_weight(packed, scales)
     n, kh = packed.shape
     k = kh * 2
     if nrows is None:
         nrows = n - row0
+    _check_range(row0, nrows, n)
     out = np.empty((nrows, k), dtype=np.float64)
     lib().oracle_dequant_rows(_ptr(packed, _u8p), _ptr(scales, _u8p), float(g), k,
                               row0, nrows, _ptr(out, _f64p))
@@ -215,11 +238,13 @@ def rmsnorm_concat(segments, m):
     parts = []
     for x, gamma, eps in segments:
         x = _c(x, np.uint16)
+        _need(x.ndim == 2 and x.shape[0] >= m, f"a segment needs {m} rows")
         ks = x.shape[1]
         out = np.empty((m, ks), dtype=np.uint16)
         gp = None
         if gamma is not None:
-            gamma = _c(gamma, np.uint16)
+            gamma = _c(gamma, np.uint16).ravel()
+            _need(gamma.size >= ks, f"gamma needs {ks} elements")
             gp = _ptr(gamma, _u16p)
         for r in range(m):
             lib().oracle_rmsnorm_row(_ptr(x[r], _u16p), ks, gp, float(eps),
@@ -233,11 +258,14 @@ def rmsnorm_concat(segments, m):
 def gemv(a_bits, packed, scales, g, n0=0, nn=None):
     """Exact y[m, nn] and sabs[m, nn] for activation bits a[m, k]."""
     a = _c(a_bits, np.uint16)
+    _need(a.ndim == 2, "activations must be 2-D")
     m, k = a.shape
     packed = _c(packed, np.uint8)
     scales = _c(scales, np.uint8)
+    _check_weight(packed, scales, k)
     if nn is None:
         nn = packed.shape[0] - n0
+    _check_range(n0, nn, packed.shape[0])
     y = np.empty((m, nn), dtype=np.float64)
     s = np.empty((m, nn), dtype=np.float64)
     lib().oracle_gemv_rows(_ptr(a, _u16p), m, k, _ptr(packed, _u8p), _ptr(scales, _u8p),
@@ -253,11 +281,16 @@ def argmax(y) -> int:
 def gemm_pairs(a_bits, packed, scales, g, rows, cols):
     """Exact C[rows[p], cols[p]] and sabs for sampled output positions."""
     a = _c(a_bits, np.uint16)
+    _need(a.ndim == 2, "A must be 2-D")
     k = a.shape[1]
     packed = _c(packed, np.uint8)
     scales = _c(scales, np.uint8)
-    rows = _c(rows, np.int64)
-    cols = _c(cols, np.int64)
+    _check_weight(packed, scales, k)
+    rows = _c(rows, np.int64).ravel()
+    cols = _c(cols, np.int64).ravel()
+    _need(rows.size == cols.size, "rows and cols must pair up")
+    _need(np.all((rows >= 0) & (rows < a.shape[0])), "a row index is outside A")
+    _need(np.all((cols >= 0) & (cols < packed.shape[0])), "a column index is outside the weight")
     exact = np.empty(rows.shape, dtype=np.float64)
     sabs = np.empty(rows.shape, dtype=np.float64)
     lib().oracle_gemm_pairs(_ptr(a, _u16p), k, _ptr(packed, _u8p), _ptr(scales, _u8p),
@@ -279,6 +312,7 @@ def argmax_masked(y, mask=None) -> int:
 def top1_logprob(y, idx, mask=None) -> float:
     """y[idx] - logsumexp over the allowed tokens; NaN when none is allowed."""
     y = _c(y, np.float64)
+    _need(0 <= int(idx) < y.size, "idx outside y")
     if mask is None:
         return float(lib().oracle_top1_logprob(_ptr(y, _f64p), y.size, None, 0, int(idx)))
     mask = _c(mask, np.int32)
@@ -297,8 +331,10 @@ def fp8_quantize(w_bits, rows=None):
     """Per-row FP8 E4M3 quantisation of BF16 bits w[n, k] (all rows or the
     given ones) -> (codes [r, k] u8, row scales [r] f32)."""
     w = _c(w_bits, np.uint16)
+    _need(w.ndim == 2, "w must be 2-D")
     n, k = w.shape
-    rows = np.arange(n) if rows is None else np.asarray(rows, dtype=np.int64)
+    rows = np.arange(n) if rows is None else np.asarray(rows, dtype=np.int64).ravel()
+    _need(np.all((rows >= 0) & (rows < n)), "row index outside the weight")
     codes = np.empty((len(rows), k), dtype=np.uint8)
     scales = np.empty(len(rows), dtype=np.float32)
     for j, r in enumerate(rows):
@@ -314,9 +350,12 @@ def fp8_gemv(a_bits, codes, scales, n0=0, nn=None):
     a = _c(a_bits, np.uint16)
     m, k = a.shape
     codes = _c(codes, np.uint8)
-    scales = _c(scales, np.float32)
+    scales = _c(scales, np.float32).ravel()
+    _need(a.ndim == 2 and codes.ndim == 2 and codes.shape[1] == k, "codes must be [n, k]")
+    _need(scales.size == codes.shape[0], "one scale per weight row")
     if nn is None:
         nn = codes.shape[0] - n0
+    _check_range(n0, nn, codes.shape[0])
     y = np.empty((m, nn), dtype=np.float64)
     s = np.empty((m, nn), dtype=np.float64)
     lib().oracle_fp8_gemv_rows(_ptr(a, _u16p), m, k, _ptr(codes, _u8p), _ptr(scales, _f32p), k,
