@@ -16,9 +16,11 @@
  *
  * Conventions shared by every call:
  *   - All pointers except those documented as host pointers are DEVICE
- *     pointers owned by the caller; the library allocates no memory, keeps no
- *     global state and never synchronises: work is enqueued on ex->stream
- *     (a cudaStream_t; NULL = legacy default stream) and the call returns.
+ *     pointers owned by the caller; the library allocates no memory and never
+ *     synchronises: work is enqueued on ex->stream (a cudaStream_t; NULL =
+ *     legacy default stream) and the call returns.  Its only state is caches
+ *     (per-device SM count, per-kernel occupancy, the tensor-map encoder
+ *     entry point) and the 256-byte scratch of w4a16_gemv_argmax_noalloc.
  *   - Arguments are checked on the host before anything is enqueued; a
  *     non-zero status means nothing was launched.  NVFP4_ERR_CUDA means a
  *     launch failed after validation (the CUDA error is left for the caller's
@@ -181,7 +183,9 @@ int nvfp4_quantize(const void *w_bf16, int64_t n, int64_t k, uint8_t *packed,
  *   y             device [m, ldy] of y_dtype (F32 or BF16, round-to-nearest-even),
  *                 ldy >= w->n.
  * Workspace: none required; with W4A16_GEMV_WS_BYTES(m, w->k) bytes the
- * activations are prepared once for all CTAs (same results either way).
+ * activations are prepared once for all CTAs (both ways are within the GEMV
+ * tolerance of the exact result; they may differ from each other in the last
+ * bits, see W4A16_GEMV_WS_BYTES).
  */
 int w4a16_gemv(const w4a16_act_segment *seg, int nseg, int m, const nvfp4_weight *w,
                void *y, int y_dtype, int64_t ldy, const nvfp4_exec *ex);
