@@ -266,6 +266,38 @@ def test_quantize_scales_and_codes_against_library_rounding():
     assert np.all(((codes >> 3) == 1) == np.signbit(x))
 
 
+def test_quantize_quotients_at_codebook_midpoints():
+    """Rows whose quotients x / d land exactly on an E2M1 midpoint whose lower
+    neighbour is odd (0.75, 1.75, 3.5), so that ties-to-even decides the code
+    -- and where x * fl32(1 / d) would land one ulp below instead.  The
+    quantiser divides with a correctly rounded binary32 '/', reproduced here
+    by numpy's IEEE division; the codes must follow it."""
+    cases = [  # (global amax, block amax, values at a midpoint after division)
+        (1.109375, 0.6953125, [0.2080078125, 0.416015625]),
+        (1.109375, 0.0849609375, [0.0260009765625, 0.052001953125]),
+        (1.1640625, 1.1484375, [0.1455078125]),
+        (1.3828125, 1.1484375, [0.345703125, 0.69140625]),
+    ]
+    dec = _torch_e4m3_decode_all().astype(np.float32)
+    for amax, amax_b, xs in cases:
+        row = np.zeros(32)
+        row[0] = amax                                   # block 0 sets the global amax
+        row[16] = amax_b                                # block 1: its amax, then the values
+        row[17:17 + len(xs)] = xs
+        wb = _bf16_bits_from_f64(row[None, :])
+        packed, sc, g, _ = oracle.quantize(wb)
+        assert g == np.float32(amax) / np.float32(2688)
+        t = np.float32(amax_b) / (np.float32(6) * g)
+        assert sc[0, 1] == _torch_e4m3_encode([t])[0]
+        d = np.float32(dec[sc[0, 1]] * g)
+        q = (np.asarray(xs, dtype=np.float32) / d).astype(np.float32)   # IEEE binary32 division
+        assert np.all(np.isin(q, [0.75, 1.75, 3.5])), "the fixture must hit exact midpoints"
+        codes = np.empty(32, dtype=np.int64)
+        codes[0::2], codes[1::2] = packed[0] & 15, packed[0] >> 4
+        expect = {0.75: 2, 1.75: 4, 3.5: 6}             # ties go to the even code
+        assert [int(c) for c in codes[17:17 + len(xs)]] == [expect[float(v)] for v in q]
+
+
 # ---------------------------------------------------------------- RMSNorm
 
 def test_rmsnorm_textbook_and_constant_rows():
