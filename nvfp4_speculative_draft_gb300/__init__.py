@@ -21,6 +21,19 @@ The C library checks what it can see (null pointers, sizes, leading
 dimensions, alignment); the extents, dtypes and devices of the tensors are
 checked here, before anything is passed down, and a mismatch raises
 ValueError.
+
+Example (one draft step's LM head and the prefill GEMM; every tensor on the
+GPU, BF16 unless stated)::
+
+    import nvfp4_speculative_draft_gb300 as nd
+    head, _ = nd.nvfp4_quantize(w_lm_head)             # [n, k] -> NVFP4, load time
+    logits, token = nd.w4a16_gemv_argmax([(hidden, norm_weight, 1e-6)], head)
+    _, token, logprob = nd.w4a16_gemv_argmax_ex([(hidden, norm_weight, 1e-6)], head,
+                                                mask=nd.pack_mask(allowed), logits=False)
+    fc, _ = nd.nvfp4_quantize(w_fc)
+    h = nd.w4a16_gemv([(embed_table, g_e, 1e-6, token), (hidden, g_h, 1e-6)], fc,
+                      out_dtype=torch.bfloat16)         # embedding gathered by token
+    c = nd.w4a16_gemm(prefill_activations, fc)          # [m, k] x [n, k]^T -> [m, n]
 """
 import ctypes
 import os
