@@ -30,6 +30,16 @@
  *     up).  The library only ever writes non-zero codes there; the caller
  *     clears it.
  *   - Concurrent calls on different streams need distinct workspaces.
+ *   - Weights are load-time constants.  The GEMV calls may read the quantised
+ *     weight (codes, scales, global scale) and the segments' gamma while the
+ *     previous kernel on the stream is still finishing (programmatic dependent
+ *     launch: the next call's weight stream starts before this one ends);
+ *     activations and gather indices are read only after it completed.  So
+ *     the weight and gamma must not be written by the kernel that immediately
+ *     precedes the call on the stream -- unless that kernel is
+ *     nvfp4_quantize / fp8w_quantize, which make their output visible before
+ *     releasing dependents.  Copies (cudaMemcpy*) and any other stream
+ *     operation in between are fine.
  *   - No C++ exception crosses this interface.
  */
 #ifndef NVFP4DRAFT_H
@@ -60,10 +70,13 @@ extern "C" {
 #define NVFP4_DTYPE_F32 0
 #define NVFP4_DTYPE_BF16 1
 
-/* Largest activation batch of the GEMV calls: one MMA column per row, in
- * groups of 8 columns that share each dequantised weight fragment (1..8 rows:
- * one group; 9..16 rows: two -- the pages' batch-16 width). */
-#define W4A16_GEMV_MAX_M 16
+/* Largest activation batch of the GEMV calls (the pages' batch-16 and
+ * batch-32 draft widths).  One launch takes up to 16 rows: one MMA column per
+ * row, in groups of 8 columns that share each dequantised weight fragment;
+ * wider batches, and batches whose activations exceed one CTA's shared memory
+ * at large k, run as consecutive launches of row blocks on the caller's
+ * stream (each streams the weights once). */
+#define W4A16_GEMV_MAX_M 32
 /* Largest total K of the GEMV calls (activations are staged on chip).  The
  * FP16 activation fragments take 2 m k bytes of one CTA's shared memory next
  * to the weight ring, so large m k combinations are refused with
@@ -72,8 +85,9 @@ extern "C" {
  *   FP8 weights:   m <= 4: 16384; m = 5: 15 360; 6: 12 800; 7: 11 008; 8: 9 728;
  *                  16: 4 608 */
 #define W4A16_GEMV_MAX_K 16384
-/* Workspace of w4a16_gemv_argmax: W4A16_GEMV_MAX_M 64-bit keys + a counter.
- * Zero it once when allocated; every completed call leaves it zeroed. */
+/* Workspace of w4a16_gemv_argmax: 16 64-bit keys (one launch's rows) + a
+ * counter.  Zero it once when allocated; every completed call leaves it
+ * zeroed. */
 #define W4A16_ARGMAX_WS_BYTES 256
 /* Most CTAs a GEMV launch uses, and the workspace of w4a16_gemv_argmax_ex
  * (keys + counter, then one (max, sum) pair per CTA and batch row). */
@@ -244,10 +258,15 @@ int w4a16_gemv_argmax_ex(const w4a16_act_segment *seg, int nseg, int m, const nv
  *   cudaStream_t (NULL = legacy default stream); dev_status is nullable.
  *   m > W4A16_GEMV_MAX_M (beyond the scratch) -> NVFP4_ERR_SHAPE.
  * The first call on a device looks up the array's device address (with that
- * device current); make that first call before any stream capture.  Each call
- * clears the scratch on its stream first.  All calls share the array, so
- * calls that overlap on the GPU (other streams, other host threads) race.
- * Allocates nothing: no cudaMalloc, cudaFree or allocating library routine.
+ * device current); make that first call before any stream capture.  Under
+ * lazy module loading (the CUDA default) that first call may also load the
+ * library's device code, which allocates device memory and may synchronise:
+ * a caller with a fixed memory budget makes one call at start-up, before the
+ * budget is handed out.  The stream must belong to the current device
+ * (otherwise NVFP4_ERR_CUDA, nothing launched).  Each call clears the scratch
+ * on its stream first.  All calls share the array, so calls that overlap on
+ * the GPU (other streams, other host threads) race.  After that first call it
+ * allocates nothing: no cudaMalloc, cudaFree or allocating library routine.
  */
 int w4a16_gemv_argmax_noalloc(const w4a16_act_segment *seg, int nseg, int m,
                               const nvfp4_weight *w, float *logits, int64_t ld_logits,

@@ -51,7 +51,7 @@ STATUS_NAMES = {0: "OK", 1: "ERR_NULL", 2: "ERR_SHAPE", 3: "ERR_ALIGN", 4: "ERR_
                 5: "ERR_CUDA", 6: "ERR_TIMEOUT", 7: "ERR_NONFINITE", 8: "ERR_DTYPE", 9: "ERR_INDEX"}
 DTYPE_F32 = 0
 DTYPE_BF16 = 1
-GEMV_MAX_M = 16
+GEMV_MAX_M = 32
 GEMV_MAX_K = 16384
 ARGMAX_WS_BYTES = 256
 GEMV_MAX_CTAS = 1024
@@ -430,11 +430,15 @@ def w4a16_gemv_argmax_noalloc(segments: Sequence, weight: Nvfp4Weight,
     if dev_status is not None:
         _check_tensor(dev_status, "dev_status", torch.int32, dev, (1,))
     w = weight.c()
-    rc = load().w4a16_gemv_argmax_noalloc(
-        segs, len(segments), m, ctypes.byref(w),
-        out_logits.data_ptr() if out_logits is not None else None,
-        out_logits.stride(0) if out_logits is not None else 0, out_argmax.data_ptr(),
-        _stream(stream), dev_status.data_ptr() if dev_status is not None else None)
+    # the library takes the scratch of the current device: make it the
+    # weight's, and default to that device's current stream
+    with torch.cuda.device(dev):
+        rc = load().w4a16_gemv_argmax_noalloc(
+            segs, len(segments), m, ctypes.byref(w),
+            out_logits.data_ptr() if out_logits is not None else None,
+            out_logits.stride(0) if out_logits is not None else 0, out_argmax.data_ptr(),
+            _stream(torch.cuda.current_stream(dev) if stream is None else stream),
+            dev_status.data_ptr() if dev_status is not None else None)
     _check("w4a16_gemv_argmax_noalloc", rc)
     return out_logits, out_argmax
 

@@ -57,6 +57,11 @@ __global__ void __launch_bounds__(kThreads) fp8_quantize_kernel(const uint4* __r
       dst[i] = make_uint2(out[0], out[1]);
     }
   }
+  // The GEMV reads its weights before its grid-dependency wait (they are
+  // load-time constants): make this kernel's output visible device-wide
+  // before a dependent launch may start.
+  __threadfence();
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 }  // namespace

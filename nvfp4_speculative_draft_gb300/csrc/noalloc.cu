@@ -11,7 +11,11 @@
 // symbol is only a stand-in.  The device address is obtained once per device
 // with cudaGetSymbolAddress, with that device current, on the first call made
 // on it; the first call on each device should therefore come before any stream
-// capture.  Each call clears the keys and counter on its stream before the
+// capture.  Under lazy module loading (the CUDA default) that first call may
+// also load the library's device code, which allocates device memory and may
+// synchronise: a caller with a fixed memory budget makes one call at start-up.
+// The stream must belong to the current device.  Each call clears the keys and
+// counter on its stream before the
 // kernel runs.  All calls share the one array: calls that overlap on the GPU
 // (concurrent streams, or several host threads) race on it.
 #include <mutex>
@@ -29,10 +33,16 @@ constexpr int kMaxDevices = 64;
 std::mutex g_mutex;
 void* g_scratch_ptr[kMaxDevices] = {nullptr};
 
-// Device address of the scratch array on the current device (set up once).
-int scratch_for_current_device(void** out) {
+// Device address of the scratch array on the current device (set up once),
+// which must also be the device of `stream`: the scratch of one device is
+// not the scratch of another.
+int scratch_for_current_device(cudaStream_t stream, void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return NVFP4_ERR_CUDA;
+  if (stream != nullptr) {
+    int sdev = -1;
+    if (cudaStreamGetDevice(stream, &sdev) != cudaSuccess || sdev != dev) return NVFP4_ERR_CUDA;
+  }
   std::lock_guard<std::mutex> lock(g_mutex);
   if (g_scratch_ptr[dev] == nullptr) {
     void* ptr = nullptr;
@@ -51,7 +61,7 @@ extern "C" int w4a16_gemv_argmax_noalloc(const w4a16_act_segment* seg, int nseg,
                                          int32_t* argmax, void* stream, int32_t* dev_status) {
   int rc = nvfp4::check_weight(w);
   if (rc) return rc;
-  // the scratch holds one key per batch row: m beyond W4A16_GEMV_MAX_M is rejected here
+  // m beyond W4A16_GEMV_MAX_M is rejected here; a launch takes at most 16 rows, one key each
   rc = nvfp4::check_segments(seg, nseg, m, w->k);
   if (rc) return rc;
   if (argmax == nullptr) return NVFP4_ERR_NULL;
@@ -60,10 +70,10 @@ extern "C" int w4a16_gemv_argmax_noalloc(const w4a16_act_segment* seg, int nseg,
     return NVFP4_ERR_ALIGN;
   if (logits != nullptr && ld_logits < w->n) return NVFP4_ERR_SHAPE;
   if (w->n > 0x7FFFFFFFLL) return NVFP4_ERR_SHAPE;
-  void* scratch = nullptr;
-  rc = scratch_for_current_device(&scratch);
-  if (rc) return rc;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  void* scratch = nullptr;
+  rc = scratch_for_current_device(st, &scratch);
+  if (rc) return rc;
   if (cudaMemsetAsync(scratch, 0, W4A16_ARGMAX_WS_BYTES, st) != cudaSuccess) return NVFP4_ERR_CUDA;
   return launch_gemv(seg, nseg, m, ref_of(w), logits, NVFP4_DTYPE_F32, ld_logits, true, argmax, scratch,
                      W4A16_ARGMAX_WS_BYTES, dev_status, st);

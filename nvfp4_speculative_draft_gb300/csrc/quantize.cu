@@ -118,6 +118,11 @@ quantize_kernel(const uint4* __restrict__ w, int64_t nblocks, const uint32_t* __
     packed[b] = make_uint2(lo, hi);
     scales[b] = (uint8_t)s;
   }
+  // The GEMV reads its weights before its grid-dependency wait (they are
+  // load-time constants): make this kernel's output visible device-wide
+  // before a dependent launch may start.
+  __threadfence();
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 }  // namespace

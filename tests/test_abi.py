@@ -70,7 +70,7 @@ def test_gemv_argument_checks(L):
     f = L.w4a16_gemv
     assert f(seg, 1, 1, ctypes.byref(w), None, 0, 256, ctypes.byref(ex)) == 1
     assert f(seg, 1, 0, ctypes.byref(w), 0x6000, 0, 256, ctypes.byref(ex)) == 2
-    assert f(seg, 1, 17, ctypes.byref(w), 0x6000, 0, 256, ctypes.byref(ex)) == 2
+    assert f(seg, 1, 33, ctypes.byref(w), 0x6000, 0, 256, ctypes.byref(ex)) == 2
     assert f(seg, 3, 1, ctypes.byref(w), 0x6000, 0, 256, ctypes.byref(ex)) == 2
     assert f(seg, 1, 1, ctypes.byref(w), 0x6000, 5, 256, ctypes.byref(ex)) == 8
     assert f(seg, 1, 1, ctypes.byref(w), 0x6000, 0, 255, ctypes.byref(ex)) == 2
@@ -124,7 +124,7 @@ def test_gemv_argmax_ex_argument_checks(L):
              ctypes.byref(ok)) == 3
     assert f(seg, 1, 1, ctypes.byref(w), 0x6000, 256, 0x7000, 0x7100, 0x7201, 8,
              ctypes.byref(ok)) == 3
-    assert f(seg, 1, 17, ctypes.byref(w), 0x6000, 256, 0x7000, 0x7100, 0x7200, 8,
+    assert f(seg, 1, 33, ctypes.byref(w), 0x6000, 256, 0x7000, 0x7100, 0x7200, 8,
              ctypes.byref(ok)) == 2
 
 

@@ -128,8 +128,9 @@ def test_lm_head_config_full(dev):
 
 
 def test_propose_config_full_width(dev):
-    """151936 x 5120 head: quantiser on sampled rows, M=1 logits + argmax over
-    every row, M=8 logits on sampled rows and argmax of the GPU's own logits."""
+    """151936 x 5120 head: quantiser on sampled rows; M = 1, 2, 4, 8 logits
+    over every row and the argmax against the oracle; grammar mask + top-1
+    log-probability at every width."""
     m = nd()
     case = workloads.propose_m8(device=dev)
     wq, amax = m.nvfp4_quantize(case.w)
@@ -160,14 +161,13 @@ def test_propose_config_full_width(dev):
     lp_ref = oracle.top1_logprob(y[0], j, mask[0])
     assert abs(float(lp[0]) - lp_ref) <= tol[i] + tol[allowed].max() + 1e-5 * (1 + abs(float(lg1[0, i])))
     for mm in (2, 4, 8):
+        # every logit of every batch row against the oracle, and the argmax by
+        # the top-2-gap rule against the oracle's index
         logits, idx = m.w4a16_gemv_argmax([(x[:mm].contiguous(), None)], wq)
         torch.cuda.synchronize()
         lg = logits.cpu().numpy()
-        ys, ss = oracle.gemv(workloads.bits(x[:mm]), pk[rows], sc[rows], g)
-        err = np.abs(lg[:, rows].astype(np.float64) - ys)
-        assert np.all(err <= TOL_REL * ss + TOL_ABS)
-        for r in range(mm):
-            assert int(idx[r]) == oracle.argmax(lg[r].astype(np.float64))
+        ys, ss = par_gemv(workloads.bits(x[:mm]), pk, sc, g)
+        check_logits_and_argmax(lg, idx.cpu().numpy(), ys, ss)
         _, idx, lp = m.w4a16_gemv_argmax_ex([(x[:mm].contiguous(), None)], wq,
                                             mask=torch.from_numpy(mask[:mm]).to(dev), logits=False)
         torch.cuda.synchronize()
@@ -200,8 +200,9 @@ def test_fc_combiner_config_full(dev, mm):
 
 
 def test_prefill_gemm_config_sampled(dev):
-    """2048 x 17408 x 5120 prefill GEMM: quantiser bit-exact on every row, and
-    8192 sampled outputs plus two full rows and two full columns."""
+    """2048 x 17408 x 5120 prefill GEMM: quantiser bit-exact on every row;
+    8192 sampled outputs, a full row in every M tile and a full column in every
+    N tile (about 320 000 outputs), on both operand paths."""
     m = nd()
     case = workloads.prefill_gemm(device=dev)
     wq, amax = m.nvfp4_quantize(case.w)
@@ -214,10 +215,17 @@ def test_prefill_gemm_config_sampled(dev):
     torch.cuda.synchronize()
     assert status.item() == 0  # no bounded wait ran out
     rng = np.random.default_rng(12)
-    rows = np.concatenate([rng.integers(0, 2048, 8192), np.full(17408, 5), np.full(17408, 2047),
-                           np.arange(2048), np.arange(2048)])
-    cols = np.concatenate([rng.integers(0, 17408, 8192), np.arange(17408), np.arange(17408),
-                           np.full(2048, 0), np.full(2048, 17407)])
+    # 8192 random outputs, one full output row inside every 256-row M tile and
+    # one full column inside every 256-column N tile (so each tile of the
+    # persistent schedule is checked along a whole row and a whole column),
+    # plus the first and last row and column
+    mt, nt = 2048 // 256, 17408 // 256
+    full_rows = np.concatenate([256 * np.arange(mt) + rng.integers(0, 256, mt), [0, 2047]])
+    full_cols = np.concatenate([256 * np.arange(nt) + rng.integers(0, 256, nt), [0, 17407]])
+    rows = np.concatenate([rng.integers(0, 2048, 8192), np.repeat(full_rows, 17408),
+                           np.tile(np.arange(2048), full_cols.size)])
+    cols = np.concatenate([rng.integers(0, 17408, 8192), np.tile(np.arange(17408), full_rows.size),
+                           np.repeat(full_cols, 2048)])
     ab = workloads.bits(case.a)
     pk, sc = wq.packed.cpu().numpy(), wq.scales.cpu().numpy()
     parts = np.array_split(np.arange(rows.size), THREADS)

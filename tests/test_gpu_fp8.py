@@ -128,29 +128,10 @@ def test_fp8_gathered_segment_and_prepared_activations(dev):
     assert np.all(np.abs(y_g.cpu().numpy().astype(np.float64) - y) <= TOL_REL * sabs + TOL_ABS)
 
 
-@pytest.mark.parametrize("m_rows,k_max", [(4, 16384), (8, 9728), (16, 4608)])
-def test_fp8_gemv_at_the_activation_size_limit(dev, m_rows, k_max):
-    from test_gpu_parity import run_at_size_limit
-    run_at_size_limit(dev, m_rows, k_max, fp8=True)
-
-
-def test_activation_footprint_limit_is_a_shape_error(dev):
-    """m * k beyond what one CTA's shared memory holds is refused (no launch)."""
-    m = nd()
-    w = torch.zeros((32, 10240), dtype=torch.bfloat16, device=dev)
-    q8 = m.fp8w_quantize(w)
-    x = torch.zeros((8, 10240), dtype=torch.bfloat16, device=dev)
-    with pytest.raises(m.Nvfp4Error) as e:
-        m.fp8w_gemv([(x, None)], q8, prepare=False)
-    assert e.value.status == 2
-    w2 = torch.zeros((32, 16384), dtype=torch.bfloat16, device=dev)
-    q4, _ = m.nvfp4_quantize(w2)
-    x2 = torch.zeros((8, 16384), dtype=torch.bfloat16, device=dev)
-    with pytest.raises(m.Nvfp4Error) as e:
-        m.w4a16_gemv([(x2, None)], q4, prepare=False)
-    assert e.value.status == 2
-    m.w4a16_gemv([(x2[:5].contiguous(), None)], q4)  # m = 5 fits at k = 16384
-    torch.cuda.synchronize()
+@pytest.mark.parametrize("m_rows,k", [(4, 16384), (8, 16384), (16, 10240), (32, 10240)])
+def test_fp8_gemv_wide_batches_at_large_k(dev, m_rows, k):
+    from test_gpu_parity import run_wide
+    run_wide(dev, m_rows, k, fp8=True)
 
 
 def test_fp8_quantize_exact_midpoint_ties(dev):

@@ -189,20 +189,22 @@ def test_gemv_two_column_groups(dev, m_rows):
         check_logits(out.cpu().numpy(), y, sabs)
 
 
-def run_at_size_limit(dev, m_rows, k_max, fp8):
-    """RMSNorm + GEMV + argmax at the largest k one batch width can stage
-    (the limits listed in the header), through both activation paths, on a
-    ragged number of weight rows; then the refusal 32 columns past it."""
+def run_wide(dev, m_rows, k, fp8):
+    """RMSNorm + GEMV + argmax for wide batches at large k, on a ragged number
+    of weight rows: batches whose activations do not fit one CTA's shared
+    memory (and every batch over 16 rows) run as consecutive row blocks, each
+    against the oracle.  Then the refusals: k past W4A16_GEMV_MAX_K and m past
+    W4A16_GEMV_MAX_M."""
     m = nd()
-    g = torch.Generator().manual_seed(m_rows * 100000 + k_max)
+    g = torch.Generator().manual_seed(m_rows * 100000 + k)
     n = 70
-    w = (torch.randn((n, k_max), generator=g) * 0.02).to(torch.bfloat16)
-    x = torch.randn((m_rows, k_max), generator=g).to(torch.bfloat16)
-    gamma = (1 + 0.05 * torch.randn(k_max, generator=g)).to(torch.bfloat16)
+    w = (torch.randn((n, k), generator=g) * 0.02).to(torch.bfloat16)
+    x = torch.randn((m_rows, k), generator=g).to(torch.bfloat16)
+    gamma = (1 + 0.05 * torch.randn(k, generator=g)).to(torch.bfloat16)
     a = oracle.rmsnorm_concat([(workloads.bits(x), workloads.bits(gamma), 1e-6)], m_rows)
     if fp8:
         codes, scales = oracle.fp8_quantize(workloads.bits(w))
-        wq = m.Fp8Weight(torch.from_numpy(codes).to(dev), torch.from_numpy(scales).to(dev), n, k_max)
+        wq = m.Fp8Weight(torch.from_numpy(codes).to(dev), torch.from_numpy(scales).to(dev), n, k)
         y, sabs = oracle.fp8_gemv(a, codes, scales)
         gemv, gemv_argmax, quantize = m.fp8w_gemv, m.fp8w_gemv_argmax, m.fp8w_quantize
     else:
@@ -212,23 +214,29 @@ def run_at_size_limit(dev, m_rows, k_max, fp8):
         gemv, gemv_argmax = m.w4a16_gemv, m.w4a16_gemv_argmax
         quantize = lambda t: m.nvfp4_quantize(t)[0]  # noqa: E731
     segs = [(x.to(dev), gamma.to(dev), 1e-6)]
-    logits, idx = gemv_argmax(segs, wq)                  # once-per-call preparation (m >= 2)
-    y_cta = gemv(segs, wq, prepare=False)                 # every CTA normalises itself
+    logits, idx = gemv_argmax(segs, wq)
+    yb = gemv(segs, wq, out_dtype=torch.bfloat16)
     torch.cuda.synchronize()
     lg = logits.cpu().numpy()
     check_logits(lg, y, sabs)
-    check_logits(y_cta.cpu().numpy(), y, sabs)
     check_argmax(idx.cpu().numpy(), lg, y, sabs)
-    w2 = quantize(torch.zeros((32, k_max + 32), dtype=torch.bfloat16, device=dev))
-    x2 = torch.zeros((m_rows, k_max + 32), dtype=torch.bfloat16, device=dev)
+    got = yb.float().cpu().numpy().astype(np.float64)
+    assert np.all(np.abs(got - y) <= TOL_REL * sabs + TOL_ABS + np.abs(y) * 2.0 ** -8)
+    kk = m.GEMV_MAX_K + 32
+    w2 = quantize(torch.zeros((32, kk), dtype=torch.bfloat16, device=dev))
+    x2 = torch.zeros((m_rows, kk), dtype=torch.bfloat16, device=dev)
     with pytest.raises(m.Nvfp4Error) as e:
-        gemv([(x2, None)], w2, prepare=False)
+        gemv([(x2, None)], w2)
     assert e.value.status == 2  # NVFP4_ERR_SHAPE
+    x3 = torch.zeros((m.GEMV_MAX_M + 1, k), dtype=torch.bfloat16, device=dev)
+    with pytest.raises(m.Nvfp4Error) as e:
+        gemv([(x3, None)], wq)
+    assert e.value.status == 2
 
 
-@pytest.mark.parametrize("m_rows,k_max", [(5, 16384), (8, 11776), (16, 5632)])
-def test_gemv_at_the_activation_size_limit(dev, m_rows, k_max):
-    run_at_size_limit(dev, m_rows, k_max, fp8=False)
+@pytest.mark.parametrize("m_rows,k", [(5, 16384), (8, 16384), (16, 10240), (24, 5120), (32, 10240)])
+def test_gemv_wide_batches_at_large_k(dev, m_rows, k):
+    run_wide(dev, m_rows, k, fp8=False)
 
 
 @pytest.mark.parametrize("n,k", [(16, 32), (17, 64), (100, 96), (257, 224), (2003, 1056)])
