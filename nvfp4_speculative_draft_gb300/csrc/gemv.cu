@@ -120,6 +120,8 @@ struct GemvParams {
   int early_trigger;  // let the next grid launch at the top instead of after the prologue
   int interleave;     // CTA b takes tiles b, b + grid, ... (else a contiguous range)
   int scale_tma;      // NVFP4 block scales arrive by TMA with the codes (k % 256 == 0)
+  int prewait;        // M = 1: ring stages issued before the grid-dependency wait
+  int l2_ahead;       // items past the ring each warp prefetches into L2 at the start
   // shared-memory carve-up (bytes from the 1 KB-aligned base)
   uint32_t off_frag, off_zero, off_part, off_tcnt, off_small, off_kred, off_bar;
 };
@@ -612,34 +614,51 @@ __device__ __forceinline__ void build_fragments(const GemvParams& p, unsigned ch
 
 // M = 1 with block columns: normalise the row into the block-column operand
 // layout (see kBcChunkBytes).  Each thread reads its 8-element groups of x and
-// gamma once, in one round trip (at most kG groups, held in registers across
-// the statistics); the statistics are reduced per warp, then by warp 0 over
-// the warps in a fixed order.
+// gamma once, in one round trip (held in registers across the statistics);
+// the statistics are reduced per warp, then by warp 0 over the warps in a
+// fixed order.
+// Registers of the M = 1 prologue: this thread's 8-element groups of x and
+// gamma (at most kBcG of them).
 template <int WARPS>
-__device__ __forceinline__ void build_bc(const GemvParams& p, unsigned char* frag, float* small, int nchunks) {
-  constexpr int kThreads = WARPS * 32;
-  constexpr int kG = (W4A16_GEMV_MAX_K / 8 + kThreads - 1) / kThreads;  // groups per thread
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  float* rms = small;
-  unsigned int* rowmax = reinterpret_cast<unsigned int*>(small + kSmallRowmax);
-  float* part = small + kSmallParts;  // [warp][6]: sum of squares, max |x|, max |gamma| per segment
+struct BcRegs {
+  static constexpr int kG = (W4A16_GEMV_MAX_K / 8 + WARPS * 32 - 1) / (WARPS * 32);
+  uint4 xv[kG], gv[kG];
+};
+
+// First half of the M = 1 prologue: issue this thread's loads of x and gamma
+// (one round trip; nothing here waits for them).
+template <int WARPS>
+__device__ __forceinline__ void build_bc_load(const GemvParams& p, BcRegs<WARPS>& r) {
+  constexpr int kThreads = WARPS * 32, kG = BcRegs<WARPS>::kG;
+  const int tid = threadIdx.x;
   const __nv_bfloat16* xr0 = seg_row(p, 0, 0);
   const __nv_bfloat16* xr1 = p.nseg == 2 ? seg_row(p, 1, 0) : xr0;
-  // x and gamma of this thread's groups: one round trip, held in registers
-  uint4 xv[kG], gv[kG];
 #pragma unroll
   for (int i = 0; i < kG; ++i) {
     const int kk = 8 * (tid + i * kThreads);
-    xv[i] = make_uint4(0u, 0u, 0u, 0u);
-    gv[i] = make_uint4(0u, 0u, 0u, 0u);
+    r.xv[i] = make_uint4(0u, 0u, 0u, 0u);
+    r.gv[i] = make_uint4(0u, 0u, 0u, 0u);
     if (kk < p.k) {
       const int s = (p.nseg == 2 && kk >= p.kseg[0]) ? 1 : 0;
       const int ko = kk - (s ? (int)p.kseg[0] : 0);
       if (!NVFP4_GUARD(ko + 8 <= p.kseg[s], 2, p.dev_status)) continue;
-      xv[i] = *reinterpret_cast<const uint4*>((s ? xr1 : xr0) + ko);
-      if (p.gamma[s] != nullptr) gv[i] = *reinterpret_cast<const uint4*>(p.gamma[s] + ko);
+      r.xv[i] = *reinterpret_cast<const uint4*>((s ? xr1 : xr0) + ko);
+      if (p.gamma[s] != nullptr) r.gv[i] = *reinterpret_cast<const uint4*>(p.gamma[s] + ko);
     }
   }
+}
+
+// Second half: statistics, normalisation and the block-column layout.
+template <int WARPS>
+__device__ __forceinline__ void build_bc(const GemvParams& p, unsigned char* frag, float* small, int nchunks,
+                                         const BcRegs<WARPS>& r) {
+  constexpr int kThreads = WARPS * 32, kG = BcRegs<WARPS>::kG;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  float* rms = small;
+  unsigned int* rowmax = reinterpret_cast<unsigned int*>(small + kSmallRowmax);
+  float* part = small + kSmallParts;  // [warp][6]: sum of squares, max |x|, max |gamma| per segment
+  const uint4* xv = r.xv;
+  const uint4* gv = r.gv;
   float ss[2] = {0.f, 0.f};
   uint32_t mx[2] = {0u, 0u}, mg[2] = {0u, 0u};
 #pragma unroll
@@ -771,7 +790,7 @@ __global__ void __launch_bounds__(512) act_prep_kernel(const __grid_constant__ G
 // Template: M batch rows (1..8 exact; 16 = any 9..16), WARPS per CTA, weight
 // format, and the block-column path (M = 1, NVFP4).
 template <int M, int WARPS, bool FP8, bool BC>
-__global__ void __launch_bounds__(WARPS * 32, (M == 1 && WARPS == 16) ? 2 : 1)
+__global__ void __launch_bounds__(WARPS * 32, 1)
 gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_s,
             const __grid_constant__ GemvParams p) {
   constexpr int MC = M > 8 ? 8 : M, NCG = (M + 7) / 8, GSTRIDE = 4 * MC, BSTRIDE = GSTRIDE * NCG;
@@ -860,14 +879,45 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
       if (++lj < nunits) set_unit(lj);
     }
   };
+  // L2 prefetch of this warp's items total_issued .. + p.l2_ahead - 1 (a hint:
+  // it fills HBM's idle time while the activations are prepared)
+  auto prefetch_ahead = [&](int from) {
+    if (lane != 0 || p.l2_ahead <= 0) return;
+    int j = lj, i = li, ib = l_ib, len = l_len, tl = l_tile;  // the load cursor, copied
+    (void)from;
+    for (int q = 0; q < p.l2_ahead && j < nunits; ++q) {
+      const int item = ib + i;
+      if constexpr (FP8) {
+        asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global [%0, {%1, %2}];" ::"l"(
+                         reinterpret_cast<uint64_t>(&tmap_w)), "r"(item * 256), "r"(tl * 16) : "memory");
+      } else {
+        asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global [%0, {%1, %2}];" ::"l"(
+                         reinterpret_cast<uint64_t>(&tmap_w)), "r"(item * 128), "r"(tl * 16) : "memory");
+        if (p.scale_tma)
+          asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global [%0, {%1, %2}];" ::"l"(
+                           reinterpret_cast<uint64_t>(&tmap_s)), "r"(item * 16), "r"(tl * 16) : "memory");
+      }
+      if (++i == len) {
+        i = 0;
+        if (++j < nunits) {
+          const int u = warp + WARPS * j, kp = u % ks;
+          ib = kp_begin(kp);
+          len = kp_begin(kp + 1) - ib;
+          tl = tile0 + tstep * (u / ks);
+        }
+      }
+    }
+  };
   __syncthreads();  // barriers initialised, tile counters zeroed
 
   // ---- before the grid-dependency wait: the weights, their scales and the
   // norm weights are load-time constants.  Start this warp's weight stream and
   // take the norm weights' maxima.
+  // M = 1: the first p.prewait ring stages go out now, the rest right after the
+  // activation loads are issued (so those loads are not queued behind them)
 #pragma unroll
   for (int i = 0; i < S; ++i)
-    if (i < total) issue(i);
+    if (i < total && (!BC || i < p.prewait)) issue(i);
   if (!prepped && !BC) gamma_max_partials<WARPS>(p, small);
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
@@ -887,7 +937,13 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
     }
     if (!mbar_wait(fbar, 0u, p.dev_status)) failed_at = 0;
   } else if constexpr (BC) {
-    build_bc<WARPS>(p, frag, small, nchunks_frag);
+    BcRegs<WARPS> br;
+    build_bc_load<WARPS>(p, br);
+#pragma unroll
+    for (int i = 0; i < S; ++i)
+      if (i < total && i >= p.prewait) issue(i);
+    prefetch_ahead(S);
+    build_bc<WARPS>(p, frag, small, nchunks_frag, br);
   } else {
     build_fragments<M, WARPS, BC>(p, frag, small, 0, MM, nchunks_frag, nullptr);
   }
@@ -1286,10 +1342,8 @@ PrepFn prep_for(int m) {
   }
 }
 
-// The block-column kernel (m = 1, NVFP4) with 32 or 16 warps.
-KernelFn bc_kernel(int warps) {
-  return warps == 32 ? gemv_kernel<1, 32, false, true> : gemv_kernel<1, 16, false, true>;
-}
+// The block-column kernel (m = 1, NVFP4).
+KernelFn bc_kernel() { return gemv_kernel<1, 16, false, true>; }
 
 template <int WARPS, bool FP8>
 KernelFn kernel_for(int m) {
@@ -1361,14 +1415,14 @@ int launch_rows(const GemvParams& base, const WeightRef& w, cudaStream_t stream,
   KernelFn fn = nullptr;
   Layout lay{};
   int warps = 0;
-  // Block columns (m = 1): 32-warp CTAs while a CTA has at most 16 tiles (a
-  // short GEMV such as the LM head: more warps shorten it); 16-warp CTAs for
-  // long streams (measured faster there: fewer copies in flight per SM).
-  const int bc_warps = p.tpc <= 16 ? 32 : 16;
-  for (int wv : {bc ? bc_warps : 16, bc ? 16 : 8}) {
+  // 16 warps of up to 128 registers (one CTA per SM; 32 warps at 64
+  // registers and 2 CTAs of 16 warps both measured slower), or 8 warps when
+  // the activations leave too little shared memory for 16 rings
+  for (int wv : {16, 8}) {
+    if (bc && wv != 16) break;
     const int ks = std::max(1, std::min({wv / p.tpc, p.nitems, kMaxKs}));
     const Layout l = layout_for(wv, m, nchunks, w.fp8, bc, ks > 1 ? p.tpc * ks : 0);
-    KernelFn f = bc ? bc_kernel(wv)
+    KernelFn f = bc ? bc_kernel()
                : wv == 16 ? (w.fp8 ? kernel_for<16, true>(m) : kernel_for<16, false>(m))
                           : (w.fp8 ? kernel_for<8, true>(m) : kernel_for<8, false>(m));
     if (nvfp4::occupancy(reinterpret_cast<const void*>(f), wv * 32, l.bytes) >= 1) {
@@ -1402,6 +1456,8 @@ int launch_rows(const GemvParams& base, const WeightRef& w, cudaStream_t stream,
   p.off_bar = lay.off_bar;
   p.early_trigger = 0;
   p.interleave = 0;
+  p.prewait = 0;
+  p.l2_ahead = 0;
 
   CUtensorMap tmap;
   const int64_t row_bytes = w.fp8 ? w.k : w.k / 2;
