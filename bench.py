@@ -349,13 +349,13 @@ def bench_details(dev, stream, hbm, bf16):
     import workloads
     out = {}
     # batched propose: 151936 x 5120 (437.6 MB of weights > L2)
-    case = workloads.propose_m8(m=16, device=dev)
+    case = workloads.propose_m8(m=32, device=dev)
     wq, _ = nd.nvfp4_quantize(case.w)
     case_w = case.w  # kept for the FP8 variant below
     del case.w
     x = case.segments[0][0]
     prop = {}
-    for m in (1, 2, 4, 8, 16):
+    for m in (1, 2, 4, 8, 16, 32):
         logits = torch.empty((m, 151936), dtype=torch.float32, device=dev)
         idx = torch.empty((m,), dtype=torch.int32, device=dev)
         xs = x[:m].contiguous()
@@ -397,6 +397,20 @@ def bench_details(dev, stream, hbm, bf16):
     ms = time_graph(chain, stream, 5) / steps
     b = gemv_bytes(5120, 10240, 1, nseg_gamma_k=10240, out_bytes_per=2, argmax=False) \
         + gemv_bytes(151936, 5120, 1, nseg_gamma_k=5120, out_bytes_per=0)
+    # the same step 16 drafts wide (the pages' batch-16 width): 16 tokens
+    # gather 16 embedding rows, fc and LM head run on 16 rows
+    tok16 = torch.randint(0, 151936, (16,), generator=gen, device=dev, dtype=torch.int64).to(torch.int32)
+    h16 = [torch.randn((16, 5120), generator=gen, device=dev).to(torch.bfloat16),
+           torch.empty((16, 5120), dtype=torch.bfloat16, device=dev)]
+
+    def chain16():
+        for i in range(steps):
+            hid, ybuf = h16[i % 2], h16[(i + 1) % 2]
+            nd.w4a16_gemv([(emb, ge, 1e-6, tok16), (hid, gh, 1e-6)], fcw, out=ybuf, stream=stream)
+            nd.w4a16_gemv_argmax([(ybuf, gf, 1e-6)], wq, logits=False, out_argmax=tok16, stream=stream)
+    ms16 = time_graph(chain16, stream, 5) / steps
+    b16 = gemv_bytes(5120, 10240, 16, nseg_gamma_k=10240, out_bytes_per=2, argmax=False) \
+        + gemv_bytes(151936, 5120, 16, nseg_gamma_k=5120, out_bytes_per=0)
     # FP8 weight variant of the same head (1 byte per weight + 4 per row)
     fp8 = {}
     w8 = nd.fp8w_quantize(case_w)
@@ -420,7 +434,11 @@ def bench_details(dev, stream, hbm, bf16):
                                    "note": "fc (embedding gathered by the previous token on "
                                            "the device) + LM head + argmax, M=1, graph of "
                                            f"{steps} chained steps"}
-    del wq, fcw, emb, hbuf
+    out["chained_propose_step_16"] = {"us_per_step": ms16 * 1e3, "GBps": b16 / ms16 / 1e6,
+                                      "frac_of_measured_hbm": b16 / ms16 / 1e6 / hbm,
+                                      "note": "the same step 16 drafts wide (16 gathered tokens; "
+                                              f"fc and LM head on 16 rows), graph of {steps} steps"}
+    del wq, fcw, emb, hbuf, h16
     # fc combiner 5120 x 10240 (29.5 MB: rotate copies)
     base = workloads.fc_combiner(device=dev)
     wbytes = 5120 * 10240 // 2 + 5120 * 10240 // 16
@@ -642,6 +660,14 @@ def main():
         cb = OracleLmHead().baseline()
         cb.pop("s_per_call", None)
         line["cpu_baseline"] = cb
+    if "detail" in line:  # the key fractions again, last, where a log tail keeps them
+        d = line["detail"]
+        summ = {f"propose_{k}": round(v["frac_of_measured_hbm"], 3)
+                for k, v in d["propose_151936x5120"].items()}
+        summ["fc_M8"] = round(d["fc_5120x10240"]["M8"]["frac_of_measured_hbm"], 3)
+        summ["gemm_bf16"] = round(d["gemm_2048x17408x5120"]["frac_of_measured_bf16"], 3)
+        summ["lm_head"] = round(line["roofline"]["frac"], 3)
+        line["summary_frac_of_measured"] = summ
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist_on:

@@ -18,6 +18,10 @@ OUT = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT, "libnvfp4draft.so")
 # Variant with device-side bounds checks on every access (see common.cuh).
 DEBUG_LIB = os.path.join(OUT, "libnvfp4draft_debug.so")
+# Test variant whose kernels withhold one copy, so a bounded wait runs out (the
+# timeout tests load it; see NVFP4_TEST_WITHHOLD in common.cuh).  Built with
+# the library.
+WITHHOLD_LIB = os.path.join(OUT, "libnvfp4draft_withhold.so")
 INCLUDE = os.path.join(ROOT, "include")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE,
@@ -40,13 +44,26 @@ def _stale(srcs, target):
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force=False, verbose=False, extra=(), debug=False):
+def build(force=False, verbose=False, extra=(), debug=False, withhold=False):
+    if not debug and not withhold:
+        # the library and its timeout-test variant, side by side
+        with cf.ThreadPoolExecutor(2) as ex:
+            fw = ex.submit(build, force, verbose, extra, False, True)
+            lib = _build_one(force, verbose, extra, False, False)
+            fw.result()
+        return lib
+    return _build_one(force, verbose, extra, debug, withhold)
+
+
+def _build_one(force, verbose, extra, debug, withhold):
     os.makedirs(OUT, exist_ok=True)
     srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
-    lib = DEBUG_LIB if debug else LIB
-    tag = "_debug" if debug else ""
+    lib = DEBUG_LIB if debug else (WITHHOLD_LIB if withhold else LIB)
+    tag = "_debug" if debug else ("_withhold" if withhold else "")
     if debug:
         extra = tuple(extra) + ("-DNVFP4_DEBUG_BOUNDS",)
+    if withhold:
+        extra = tuple(extra) + ("-DNVFP4_TEST_WITHHOLD",)
     if not force and not _stale(srcs, lib):
         return lib
     nvcc = _nvcc()

@@ -30,6 +30,19 @@ __device__ __forceinline__ bool guard(bool ok, int tag, int32_t* st) {
 #define NVFP4_GUARD(cond, tag, st) true
 #endif
 
+// Test build (-DNVFP4_TEST_WITHHOLD, the library the timeout tests load): CTA 0
+// never issues one copy -- the GEMV's warp 0 its first weight stage, the
+// GEMM's producer its first A tile -- so the bounded wait on it runs out (the
+// limit is 20 ms there) and the unwinding after a timeout runs.  Nothing of
+// the withheld copy is ever in flight.
+#ifdef NVFP4_TEST_WITHHOLD
+constexpr unsigned long long kWaitLimit = 20000000ull;  // ns of globaltimer
+constexpr bool kWithhold = true;
+#else
+constexpr unsigned long long kWaitLimit = 2000000000ull;
+constexpr bool kWithhold = false;
+#endif
+
 __host__ __device__ __forceinline__ int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }

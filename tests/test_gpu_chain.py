@@ -109,3 +109,53 @@ def test_chained_propose_steps_match_oracle(dev):
             assert i == j
         else:
             assert lx[0, i] >= lx[0, j] - tol[0, i] - tol[0, j]
+
+
+@pytest.mark.parametrize("m_rows", [16, 32])
+def test_chained_propose_steps_wide_batches(dev, m_rows):
+    """The chained step at the batch-16 and batch-32 draft widths with the
+    draft head's widths: fc 5120 x 10240 over [norm(embed[token]),
+    norm(hidden)] (k = 10240), LM head over norm_f(hidden) (k = 5120, a 1024
+    token vocabulary); each batch row's token feeds its own gather.  Two
+    steps, every output against the oracle."""
+    from test_gpu_configs import par_gemv
+    m = nd()
+    V, H = 1024, 5120
+    emb = rand_bf16((V, H), 1.0, 20, dev)
+    ge, gh, gf = (rand_bf16((H,), 0.05, s, dev, 1.0) for s in (21, 22, 23))
+    fc, _ = m.nvfp4_quantize(rand_bf16((H, 2 * H), 0.015, 24, dev))
+    lm, _ = m.nvfp4_quantize(rand_bf16((V, H), 0.02, 25, dev))
+    g = torch.Generator().manual_seed(26)
+    tok = torch.randint(0, V, (m_rows,), generator=g, dtype=torch.int32).to(dev)
+    hid = rand_bf16((m_rows, H), 1.0, 27, dev)
+    steps = []
+    for _ in range(2):
+        y = m.w4a16_gemv([(emb, ge, 1e-6, tok), (hid, gh, 1e-6)], fc, out_dtype=torch.bfloat16)
+        logits, nxt = m.w4a16_gemv_argmax([(y, gf, 1e-6)], lm)
+        steps.append((tok.clone(), hid.clone(), y.clone(), logits.clone(), nxt.clone()))
+        tok, hid = nxt, y
+    torch.cuda.synchronize()
+    b = workloads.bits
+    fcp, fcs, fcg = fc.packed.cpu().numpy(), fc.scales.cpu().numpy(), np.float32(fc.global_scale.item())
+    lmp, lms, lmg = lm.packed.cpu().numpy(), lm.scales.cpu().numpy(), np.float32(lm.global_scale.item())
+    for t, h, y, logits, nxt in steps:
+        e = emb[t.long()].cpu()
+        a = oracle.rmsnorm_concat([(b(e), b(ge.cpu()), 1e-6), (b(h.cpu()), b(gh.cpu()), 1e-6)], m_rows)
+        yx, ys = par_gemv(a, fcp, fcs, fcg)
+        got = y.float().cpu().numpy().astype(np.float64)
+        assert np.all(np.abs(got - yx) <= TOL_REL * ys + TOL_ABS + np.abs(yx) * 2.0 ** -8)
+        a2 = oracle.rmsnorm_concat([(b(y.cpu()), b(gf.cpu()), 1e-6)], m_rows)
+        lx, ls = par_gemv(a2, lmp, lms, lmg)
+        lg = logits.cpu().numpy().astype(np.float64)
+        tol = TOL_REL * ls + TOL_ABS
+        assert np.all(np.abs(lg - lx) <= tol)
+        for r in range(m_rows):
+            i = int(nxt[r].item())
+            assert i == oracle.argmax(lg[r])
+            j = oracle.argmax(lx[r])
+            order = np.argsort(-lx[r], kind="stable")
+            second = order[1] if order[0] == j else order[0]
+            if lx[r, j] - lx[r, second] > tol[r, j] + tol[r, second]:
+                assert i == j
+            else:
+                assert lx[r, i] >= lx[r, j] - tol[r, i] - tol[r, j]

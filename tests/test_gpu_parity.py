@@ -234,7 +234,8 @@ def run_wide(dev, m_rows, k, fp8):
     assert e.value.status == 2
 
 
-@pytest.mark.parametrize("m_rows,k", [(5, 16384), (8, 16384), (16, 10240), (24, 5120), (32, 10240)])
+@pytest.mark.parametrize("m_rows,k", [(5, 16384), (8, 16384), (16, 10240), (16, 5120), (24, 5120),
+                                        (32, 5120), (32, 10240)])
 def test_gemv_wide_batches_at_large_k(dev, m_rows, k):
     run_wide(dev, m_rows, k, fp8=False)
 
