@@ -77,13 +77,10 @@ extern "C" {
  * at large k, run as consecutive launches of row blocks on the caller's
  * stream (each streams the weights once). */
 #define W4A16_GEMV_MAX_M 32
-/* Largest total K of the GEMV calls (activations are staged on chip).  The
+/* Largest total K of the GEMV calls (activations are staged on chip: the
  * FP16 activation fragments take 2 m k bytes of one CTA's shared memory next
- * to the weight ring, so large m k combinations are refused with
- * NVFP4_ERR_SHAPE.  Largest k per batch width (9..16 rows count as 16):
- *   NVFP4 weights: m <= 5: 16384; m = 6: 15 616; 7: 13 312; 8: 11 776; 16: 5 632
- *   FP8 weights:   m <= 4: 16384; m = 5: 15 360; 6: 12 800; 7: 11 008; 8: 9 728;
- *                  16: 4 608 */
+ * to the weight ring; a batch whose fragments do not fit runs as row blocks of
+ * 8, 4, ... rows, so every m <= W4A16_GEMV_MAX_M runs at every k up to this). */
 #define W4A16_GEMV_MAX_K 16384
 /* Workspace of w4a16_gemv_argmax: 16 64-bit keys (one launch's rows) + a
  * counter.  Zero it once when allocated; every completed call leaves it

@@ -12,12 +12,12 @@ Recipe (the pages print no dataset; every input is synthetic):
   * lm_head_m1   (32768 x 4096 reduced-vocab LM head, M=1 with RMSNorm):
     W ~ N(0, 0.02) with round(0.01 N) rows, picked by a seeded permutation,
     multiplied by 8; gamma = 1 + N(0, 0.05); H[1000, 4096] ~ N(0, 1); eps 1e-6.
-  * propose_m8   (151936 x 5120 LM head, no norm; M in 1..8, and 16 for the
-    batch-16 draft width): W ~ N(0, 0.02) with every 16-element K block
+  * propose_m8   (151936 x 5120 LM head, no norm; M in 1..8, and 16 / 32 for
+    the batch-16 and batch-32 draft widths): W ~ N(0, 0.02) with every 16-element K block
     multiplied by 2^u, u ~ U[-6, 2] per block; X[m, 5120] ~ N(0, 1), m = 8
     by default (a call at batch M uses rows 0..M-1).
   * fc_combiner  (5120 x 10240 fc, two RMSNorms + concat; M in 1..8, and up
-    to 16): W ~ N(0, 0.015); E, H [m, 5120] ~ N(0, 1), m = 8 by default;
+    to 32): W ~ N(0, 0.015); E, H [m, 5120] ~ N(0, 1), m = 8 by default;
     gamma_e, gamma_h = 1 + N(0, 0.05).
   * prefill_gemm (2048 x 17408 x 5120): A ~ N(0, 1); W ~ N(0, 0.02).
   * tiny         (256 x 512, M=1): W ~ N(0, 0.02); x ~ N(0, 1).
