@@ -307,7 +307,7 @@ int w4a16_gemm(const void *a_bf16, int64_t m, int64_t lda, const nvfp4_weight *w
  *     y[m, n] = s_n * sum_i a[m, i] * e4m3(c[n, i])   (FP32 accumulation).
  *
  * fp8w_quantize -- BF16 w [n, k] (16-B aligned, k % 32 == 0) -> codes [n, k]
- *   (16-B aligned) and row_scale [n].  One CTA per row.  Non-finite input:
+ *   (16-B aligned) and row_scale [n].  One warp per row.  Non-finite input:
  *   results undefined, NVFP4_ERR_NONFINITE to dev_status.  No workspace.
  * fp8w_gemv, fp8w_gemv_argmax -- the same contracts (segments, RMSNorm +
  *   concat + gather, outputs, argmax ties, workspaces) as w4a16_gemv and

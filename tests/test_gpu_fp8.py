@@ -157,3 +157,38 @@ def test_fp8_quantize_exact_midpoint_ties(dev):
     down = torch.where(nz, bits - 1, bits).view(torch.bfloat16)
     up[:, 0], down[:, 0] = wb[:, 0], wb[:, 0]              # keep each row's maximum
     quantize_both(torch.cat([wb, up, down]), dev)
+
+
+def near_tie_rows(k=256):
+    """One row per row maximum A in [1, 2) (every BF16 value there): elements x
+    whose quotient fl32(x / s) falls within two binary32 ulps of an E4M3
+    rounding midpoint while x / s is not the midpoint (s = fl32(A / 448)
+    inexact), with their negations; the row's codes then hang on the
+    correctly rounded quotient."""
+    v = torch.arange(0, 127, dtype=torch.uint8).view(torch.float8_e4m3fn).double().numpy()
+    mids = (v[1:] + v[:-1]) / 2
+    rows, hits = [], 0
+    for a in torch.arange(0x3F80, 0x4000, dtype=torch.int16).view(torch.bfloat16).float().numpy():
+        s = np.float32(a) / np.float32(448)
+        near = torch.from_numpy(mids * float(s)).to(torch.bfloat16).view(torch.int16)
+        row = [float(a)]
+        for off in (-1, 0, 1):
+            x = (near + off).view(torch.bfloat16).float().numpy()
+            q = (x / s).astype(np.float32)
+            ul = np.spacing(mids.astype(np.float32)).astype(np.float64)
+            hit = ((np.abs(q.astype(np.float64) - mids) <= 2 * ul)
+                   & (x.astype(np.float64) != mids * float(s)) & (x <= a))
+            for i in np.nonzero(hit)[0]:
+                row += [float(x[i]), -float(x[i])]
+        hits += (len(row) - 1) // 2
+        row = row[:k] + [0.0] * max(0, k - len(row))
+        rows.append(row)
+    return torch.tensor(rows, dtype=torch.float32).to(torch.bfloat16), hits
+
+
+def test_fp8_quantize_near_tie_quotients(dev):
+    """Codes where the quotient's binary32 rounding lands on or next to an
+    E4M3 midpoint (double rounding): each must equal the oracle's."""
+    w, hits = near_tie_rows()
+    assert hits > 500, "the construction should find many near-tie quotients"
+    quantize_both(w, dev)

@@ -451,3 +451,66 @@ def test_quantize_exact_midpoint_ties(dev):
     blocks = torch.cat([wb, up, down, torch.zeros_like(wb)], dim=1)
     blocks[0, 63] = 2688.0  # the global maximum: g = 2688 / 2688 = 1 exactly
     quantize_both(blocks, dev)
+
+
+def near_tie_blocks(amax):
+    """Blocks whose quotients fl32(x / d) fall within two binary32 ulps of an
+    E2M1 rounding midpoint while x / d itself is not the midpoint (d = fl32(
+    dec(s) * g) with g = fl32(amax / 2688) inexact), plus the global maximum:
+    there the correctly rounded quotient, not the exact one, decides the code.
+    Each block holds its scale-setting maximum, the near-tie element and its
+    negation."""
+    g = np.float32(amax) / np.float32(2688)
+    dec = torch.arange(1, 127, dtype=torch.uint8).view(torch.float8_e4m3fn).float().numpy()
+    d = (dec * g).astype(np.float32)
+    blocks = []
+    for mid in (0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0):
+        near = torch.from_numpy(mid * d.astype(np.float64)).to(torch.bfloat16).view(torch.int16)
+        for off in (-2, -1, 0, 1, 2):
+            x = (near + off).view(torch.bfloat16).float().numpy()
+            q = (x / d).astype(np.float32)
+            hit = ((np.abs(q.astype(np.float64) - mid) <= 2 * np.spacing(np.float32(mid)))
+                   & (x.astype(np.float64) != mid * d.astype(np.float64)))
+            for i in np.nonzero(hit)[0]:
+                bmax = float(torch.tensor(6.0 * float(d[i])).to(torch.bfloat16))
+                blocks.append([bmax, float(x[i]), -float(x[i])] + [0.0] * 13)
+    blocks.append([amax] + [0.0] * 15)
+    if len(blocks) % 2:
+        blocks.append([0.0] * 16)
+    return torch.tensor(blocks, dtype=torch.float32).view(-1, 32).to(torch.bfloat16), len(blocks)
+
+
+@pytest.mark.parametrize("amax", [1.0, 1.03125, 1.453125, 1.78125])
+def test_quantize_near_tie_quotients(dev, amax):
+    """Codes where the quotient's binary32 rounding lands on or next to an
+    E2M1 midpoint (double rounding): each must equal the oracle's."""
+    w, nblk = near_tie_blocks(amax)
+    assert nblk > 100, "the construction should find many near-tie quotients"
+    assert float(w.float().abs().max()) == amax
+    quantize_both(w, dev)
+
+
+def test_quantize_scale_array_at_odd_address(dev):
+    """The scale array may start at any byte: an odd start takes the
+    byte-wise scale stores, with the same bytes as the oracle's and the bytes
+    around the array untouched."""
+    import ctypes
+    m = nd()
+    w = workloads.propose_m8(n=300, k=512).w
+    p, s, g, _ = oracle.quantize(workloads.bits(w))
+    n, k = w.shape
+    wd = w.to(dev).contiguous()
+    packed = torch.empty((n, k // 2), dtype=torch.uint8, device=dev)
+    buf = torch.full((n * (k // 16) + 2,), 0xA5, dtype=torch.uint8, device=dev)
+    gs = torch.empty(1, dtype=torch.float32, device=dev)
+    amax = torch.empty(1, dtype=torch.float32, device=dev)
+    ex = m._exec(None, None, None, dev)
+    rc = m.load().nvfp4_quantize(wd.data_ptr(), n, k, packed.data_ptr(), buf.data_ptr() + 1,
+                                 gs.data_ptr(), amax.data_ptr(), ctypes.byref(ex))
+    assert rc == 0
+    torch.cuda.synchronize()
+    got = buf.cpu().numpy()
+    assert got[0] == 0xA5 and got[-1] == 0xA5
+    assert np.array_equal(got[1:-1].reshape(s.shape), s)
+    assert np.array_equal(packed.cpu().numpy(), p)
+    assert gs.item() == float(g)
