@@ -272,7 +272,8 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   uint4 v;
   asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(addr));
+               : "r"(addr)
+               : "memory");  // stays after the barrier wait that makes the stage valid
   return v;
 }
 
@@ -357,11 +358,15 @@ quantize_kernel(const uint4* __restrict__ w, int64_t nblocks, const uint32_t* __
 #pragma unroll
     for (int q = 0; q < 4; ++q)
       if (q < 2 * nb) v[q] = lds128(src + 16u * q);  // vectors 2h, 2h + 1 hold block h
+    // the stage is released once every lane has used the values it read
+    // (a load's data is only certain to have left shared memory when an
+    // instruction has consumed it), then the results are stored
+    BlockCodes q0 = {make_uint2(0u, 0u), 0u}, q1 = {make_uint2(0u, 0u), 0u};
+    if (nb >= 1) q0 = quantize_block(v[0], v[1], g, six_g, fast6, t6lo, t6hi, tab);
+    if (nb == 2) q1 = quantize_block(v[2], v[3], g, six_g, fast6, t6lo, t6hi, tab);
     __syncwarp();
     if (lane == 0) mbar_arrive(empty0 + 8 * st);
     if (nb == 2) {
-      const BlockCodes q0 = quantize_block(v[0], v[1], g, six_g, fast6, t6lo, t6hi, tab);
-      const BlockCodes q1 = quantize_block(v[2], v[3], g, six_g, fast6, t6lo, t6hi, tab);
       *reinterpret_cast<uint4*>(packed + b0) = make_uint4(q0.codes.x, q0.codes.y, q1.codes.x, q1.codes.y);
       if (scales_even) {
         *reinterpret_cast<uint16_t*>(scales + b0) = (uint16_t)(q0.scale | q1.scale << 8);
@@ -370,7 +375,6 @@ quantize_kernel(const uint4* __restrict__ w, int64_t nblocks, const uint32_t* __
         scales[b0 + 1] = (uint8_t)q1.scale;
       }
     } else if (nb == 1) {
-      const BlockCodes q0 = quantize_block(v[0], v[1], g, six_g, fast6, t6lo, t6hi, tab);
       packed[b0] = q0.codes;
       scales[b0] = (uint8_t)q0.scale;
     }
