@@ -540,3 +540,35 @@ def test_quantize_repeatable_at_full_size(dev):
         p, s = oracle.quantize_rows(wb, np.array([r]), g)
         assert np.array_equal(first.scales[int(r)].cpu().numpy(), s[0])
         assert np.array_equal(first.packed[int(r)].cpu().numpy(), p[0])
+
+
+@pytest.mark.parametrize("m_rows,n,k,width", [(2048, 4864, 128, 256), (300, 512, 256, 240)])
+def test_gemm_both_tile_widths(dev, m_rows, n, k, width):
+    """The GEMM picks 256- or 240-wide tiles by the waves they fill (whole
+    waves of one CTA per SM, each tile costed as its width + 16).  2048 x 4864
+    is 152 tiles of 256 (one wave) and takes 256; 300 x 512 takes 240, whose
+    last tile holds 32 valid columns.  A full output row in every 256-row M
+    tile, a full column in every tile of the chosen width, and random samples
+    against the oracle."""
+    m = nd()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    mt = -(-m_rows // 256)
+    cost = {bn: -(-(mt * -(-n // bn)) // sms) * (bn + 16) for bn in (256, 240)}
+    if (240 if cost[240] < cost[256] else 256) != width:
+        pytest.skip(f"on {sms} SMs this shape does not select the {width}-wide tiles")
+    case = workloads.prefill_gemm(m=m_rows, n=n, k=k)
+    p, s, g, _ = oracle.quantize(workloads.bits(case.w))
+    wq = upload_weight(p, s, g, dev)
+    c = m.w4a16_gemm(case.a.to(dev), wq)
+    torch.cuda.synchronize()
+    cg = c.float().cpu().numpy()
+    rng = np.random.default_rng(width)
+    full_rows = np.minimum(256 * np.arange(mt) + rng.integers(0, 256, mt), m_rows - 1)
+    nt = -(-n // width)
+    full_cols = np.minimum(width * np.arange(nt) + rng.integers(0, width, nt), n - 1)
+    full_cols = np.concatenate([full_cols, [n - 1]])
+    rows = np.concatenate([rng.integers(0, m_rows, 4096), np.repeat(full_rows, n),
+                           np.tile(np.arange(m_rows), full_cols.size)])
+    cols = np.concatenate([rng.integers(0, n, 4096), np.tile(np.arange(n), full_rows.size),
+                           np.repeat(full_cols, m_rows)])
+    check_gemm(case.a, (p, s, g), cg, rows, cols)
