@@ -1366,6 +1366,17 @@ KernelFn kernel_for(int m) {
   }
 }
 
+// 12 warps: the 8- and 16-row kernels whose activations (160 KB at 16 rows x
+// 5120 or 8 rows x 10240) leave room for 12 rings but not 16
+template <bool FP8>
+KernelFn kernel_for12(int m) {
+  switch (m) {
+    case 8: return gemv_kernel<8, 12, FP8, false>;
+    case 16: return gemv_kernel<16, 12, FP8, false>;
+    default: return nullptr;
+  }
+}
+
 struct Layout {
   uint32_t off_frag, off_zero, off_part, off_tcnt, off_small, off_kred, off_bar;
   size_t bytes;  // dynamic shared memory to request (includes 1 KB alignment slack)
@@ -1373,7 +1384,7 @@ struct Layout {
 
 // Shared-memory carve-up: ring | activations (+ zero area) | split-K partials |
 // tile counters | prologue scratch | argmax reduction | ring barriers.
-Layout layout_for(int warps, int m, int nchunks, bool fp8, bool bc, int part_slots) {
+Layout layout_for(int warps, int m, int nchunks, bool fp8, bool bc, int part_slots, bool argmax) {
   const int S = ring_depth(fp8);
   const int cols = m <= 8 ? m : 16, ncg = (m + 7) / 8;  // the kernel's M, column groups
   Layout l;
@@ -1391,8 +1402,8 @@ Layout layout_for(int warps, int m, int nchunks, bool fp8, bool bc, int part_slo
   l.off_small = (uint32_t)off;
   off += (size_t)small_floats(warps) * sizeof(float);
   off = (off + 15) & ~(size_t)15;
-  l.off_kred = (uint32_t)off;
-  off += (size_t)warps * kMaxRows * (sizeof(unsigned long long) + sizeof(float2));
+  l.off_kred = (uint32_t)off;  // argmax reduction: only read when the call wants the argmax
+  if (argmax) off += (size_t)warps * kMaxRows * (sizeof(unsigned long long) + sizeof(float2));
   l.off_bar = (uint32_t)off;
   off += (size_t)warps * S * 8 + 8;  // ring barriers + the fragment-copy barrier
   l.bytes = off + 1024;
@@ -1422,14 +1433,18 @@ int launch_rows(const GemvParams& base, const WeightRef& w, cudaStream_t stream,
   Layout lay{};
   int warps = 0;
   // 16 warps of up to 128 registers (one CTA per SM; 32 warps at 64
-  // registers and 2 CTAs of 16 warps both measured slower), or 8 warps when
-  // the activations leave too little shared memory for 16 rings
-  for (int wv : {16, 8}) {
+  // registers and 2 CTAs of 16 warps both measured slower), or 12 (8 and 16
+  // rows) or 8 warps when the activations leave too little shared memory for
+  // 16 rings
+  for (int wv : {16, 12, 8}) {
     if (bc && wv != 16) break;
+    const int mk = m <= 8 ? m : 16;  // the kernel's M
+    if (wv == 12 && mk != 8 && mk != 16) continue;
     const int ks = std::max(1, std::min({wv / p.tpc, p.nitems, kMaxKs}));
-    const Layout l = layout_for(wv, m, nchunks, w.fp8, bc, ks > 1 ? p.tpc * ks : 0);
+    const Layout l = layout_for(wv, m, nchunks, w.fp8, bc, ks > 1 ? p.tpc * ks : 0, p.keys != nullptr);
     KernelFn f = bc ? bc_kernel()
                : wv == 16 ? (w.fp8 ? kernel_for<16, true>(m) : kernel_for<16, false>(m))
+               : wv == 12 ? (w.fp8 ? kernel_for12<true>(mk) : kernel_for12<false>(mk))
                           : (w.fp8 ? kernel_for<8, true>(m) : kernel_for<8, false>(m));
     if (nvfp4::occupancy(reinterpret_cast<const void*>(f), wv * 32, l.bytes) >= 1) {
       fn = f;
