@@ -14,10 +14,12 @@
 // byte per weight incl. scales; FP8: 1 byte + 4 per row).
 //   * Work split: one CTA per SM (grid <= SM count), each owning a contiguous,
 //     equal range of 16-row tiles, so every SM streams the same number of weight
-//     bytes.  Inside the CTA, ks warps share a tile's K range (split K) when the
-//     CTA has fewer tiles than warps; a tile's partials are summed in a fixed
-//     order by the warp that finishes last, so every tile's sum is formed the
-//     same way (equal weight rows give bit-equal logits).
+//     bytes.  Inside the CTA each warp takes a contiguous run of the CTA's
+//     work units: whole tiles, or, when the CTA has at most half as many tiles
+//     as warps, K parts of tiles (split K, ks parts per tile).  A split tile's
+//     part sums are added in K-part order once every warp has streamed its
+//     units, so every tile's sum is formed the same way (equal weight rows
+//     give bit-equal logits).
 //   * Weight stream: every warp owns a 2-stage shared-memory ring; one lane
 //     issues the TMA copy (cp.async.bulk.tensor) of a stage -- 256 K elements
 //     of 16 rows: one box of 16 rows x 128 bytes (NVFP4) or 16 x 256 bytes
@@ -115,15 +117,12 @@ struct GemvParams {
   int nitems;      // ceil(k / 256): ring stages per tile
   int tpc;         // tiles per CTA (the last CTA may have fewer)
   int ks;          // warps sharing one tile (split K), 1..16, <= nitems
+  int kbeg[kMaxKs + 1];  // first stage of K part kp: kp * nitems / ks (no division on the device)
   const uint2* frag_src;          // fragments prepared by act_prep_kernel, or null
   const unsigned int* rowmax_src; // their per-row scale carriers [16]
-  int early_trigger;  // let the next grid launch at the top instead of after the prologue
-  int interleave;     // CTA b takes tiles b, b + grid, ... (else a contiguous range)
   int scale_tma;      // NVFP4 block scales arrive by TMA with the codes (k % 256 == 0)
-  int prewait;        // M = 1: ring stages issued before the grid-dependency wait
-  int l2_ahead;       // items past the ring each warp prefetches into L2 at the start
   // shared-memory carve-up (bytes from the 1 KB-aligned base)
-  uint32_t off_frag, off_zero, off_part, off_tcnt, off_small, off_kred, off_bar;
+  uint32_t off_frag, off_zero, off_part, off_small, off_kred, off_bar;
 };
 
 // Block-column path: lanes (g, t = 0) emit rows g and g + 8 of every tile; their
@@ -132,6 +131,17 @@ struct GemvParams {
 struct BcRun {
   unsigned long long key;
   float lm, ls;
+};
+
+// (local tile, K part) of a work unit; next() steps to the following unit.
+struct UnitCursor {
+  int tl, kp;
+  __device__ __forceinline__ void next(int ks) {
+    if (++kp == ks) {
+      kp = 0;
+      ++tl;
+    }
+  }
 };
 
 // ------------------------------------------------------------ PTX helpers
@@ -810,27 +820,28 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
   unsigned char* frag = smem + p.off_frag;
   float* small = reinterpret_cast<float*>(smem + p.off_small);
   float* part = reinterpret_cast<float*>(smem + p.off_part);
-  unsigned int* tcnt = reinterpret_cast<unsigned int*>(smem + p.off_tcnt);
   unsigned long long* kred = reinterpret_cast<unsigned long long*>(smem + p.off_kred);
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, t = lane & 3;
-  if (p.early_trigger) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
-  // this CTA's tiles [tile0, tile0 + nt); its warps' units u = warp + WARPS j,
-  // unit u = (local tile u / ks, K part u % ks)
-  // tile indices fit 27 bits (checked on the host)
-  const int tile0 = p.interleave ? (int)blockIdx.x : (int)blockIdx.x * p.tpc;
-  const int tstep = p.interleave ? (int)gridDim.x : 1;
-  const int nt = p.interleave ? ((int)p.ntiles - tile0 + tstep - 1) / tstep : min(p.tpc, (int)p.ntiles - tile0);
+  // This CTA's tiles [tile0, tile0 + nt), as units u = (local tile u / ks, K
+  // part u % ks); warp w takes the contiguous units [ceil(w U / WARPS),
+  // ceil((w + 1) U / WARPS)) (warp 0 always starts at unit 0; with fewer units
+  // than warps the last warps idle).  Tile indices fit 27 bits (checked on the
+  // host).
+  const int tile0 = (int)blockIdx.x * p.tpc;
+  const int nt = min(p.tpc, (int)p.ntiles - tile0);
   const int ks = p.ks;
-  const int U = nt > 0 ? nt * ks : 0;
-  const int nunits = U > warp ? (U - 1 - warp) / WARPS + 1 : 0;
-  auto kp_begin = [&](int kp) { return (int)((int64_t)kp * p.nitems / ks); };
+  const int64_t U = nt > 0 ? (int64_t)nt * ks : 0;
+  const int ubeg = (int)(((int64_t)warp * U + WARPS - 1) / WARPS);
+  const int nunits = (int)(((int64_t)(warp + 1) * U + WARPS - 1) / WARPS) - ubeg;
+  auto kp_begin = [&](int kp) { return p.kbeg[kp]; };
+  const UnitCursor first{ubeg / ks, ubeg % ks};
   int total = 0;  // ring stages this warp streams
-  for (int j = 0; j < nunits; ++j) {
-    const int kp = (warp + WARPS * j) % ks;
-    total += kp_begin(kp + 1) - kp_begin(kp);
+  {
+    UnitCursor c = first;
+    for (int j = 0; j < nunits; ++j, c.next(ks)) total += kp_begin(c.kp + 1) - kp_begin(c.kp);
   }
   const uint32_t ring = base;  // the ring sits at the start of the carve-up (1 KB aligned)
   const uint32_t wring = ring + (uint32_t)warp * (S * kStage);
@@ -849,18 +860,17 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
     if (threadIdx.x == 0) mbar_init(fbar, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (threadIdx.x < kMaxKs) tcnt[threadIdx.x] = 0u;
   __syncwarp();
 
   // ---- load cursor over (unit, item); scale rows change once per unit
   int lj = 0, li = 0, l_ib = 0, l_len = 0, l_tile = 0;
-  auto set_unit = [&](int j) {
-    const int u = warp + WARPS * j, kp = u % ks;
-    l_ib = kp_begin(kp);
-    l_len = kp_begin(kp + 1) - l_ib;
-    l_tile = tile0 + tstep * (u / ks);
+  UnitCursor lc = first;
+  auto set_unit = [&]() {
+    l_ib = kp_begin(lc.kp);
+    l_len = kp_begin(lc.kp + 1) - l_ib;
+    l_tile = tile0 + lc.tl;
   };
-  if (nunits > 0) set_unit(0);
+  if (nunits > 0) set_unit();
   // NVFP4 block scales: with scale_tma a 16 x 16-byte box of the stage's rows
   // lands behind its codes (row r's 16 bytes: the 8 blocks of each of the two
   // chunks); otherwise a lane reads its scale pairs from global memory when it
@@ -882,48 +892,19 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
     }
     if (++li == l_len) {
       li = 0;
-      if (++lj < nunits) set_unit(lj);
+      lc.next(ks);
+      if (++lj < nunits) set_unit();
     }
   };
-  // L2 prefetch of this warp's items total_issued .. + p.l2_ahead - 1 (a hint:
-  // it fills HBM's idle time while the activations are prepared)
-  auto prefetch_ahead = [&](int from) {
-    if (lane != 0 || p.l2_ahead <= 0) return;
-    int j = lj, i = li, ib = l_ib, len = l_len, tl = l_tile;  // the load cursor, copied
-    (void)from;
-    for (int q = 0; q < p.l2_ahead && j < nunits; ++q) {
-      const int item = ib + i;
-      if constexpr (FP8) {
-        asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global [%0, {%1, %2}];" ::"l"(
-                         reinterpret_cast<uint64_t>(&tmap_w)), "r"(item * 256), "r"(tl * 16) : "memory");
-      } else {
-        asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global [%0, {%1, %2}];" ::"l"(
-                         reinterpret_cast<uint64_t>(&tmap_w)), "r"(item * 128), "r"(tl * 16) : "memory");
-        if (p.scale_tma)
-          asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global [%0, {%1, %2}];" ::"l"(
-                           reinterpret_cast<uint64_t>(&tmap_s)), "r"(item * 16), "r"(tl * 16) : "memory");
-      }
-      if (++i == len) {
-        i = 0;
-        if (++j < nunits) {
-          const int u = warp + WARPS * j, kp = u % ks;
-          ib = kp_begin(kp);
-          len = kp_begin(kp + 1) - ib;
-          tl = tile0 + tstep * (u / ks);
-        }
-      }
-    }
-  };
-  __syncthreads();  // barriers initialised, tile counters zeroed
+  __syncthreads();  // barriers initialised
 
   // ---- before the grid-dependency wait: the weights, their scales and the
   // norm weights are load-time constants.  Start this warp's weight stream and
-  // take the norm weights' maxima.
-  // M = 1: the first p.prewait ring stages go out now, the rest right after the
-  // activation loads are issued (so those loads are not queued behind them)
+  // take the norm weights' maxima.  M = 1 issues its ring stages right after
+  // the activation loads instead (so those loads are not queued behind them).
 #pragma unroll
   for (int i = 0; i < S; ++i)
-    if (i < total && (!BC || i < p.prewait)) issue(i);
+    if (i < total && !BC) issue(i);
   if (!prepped && !BC) gamma_max_partials<WARPS>(p, small);
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
@@ -947,14 +928,13 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
     build_bc_load<WARPS>(p, br);
 #pragma unroll
     for (int i = 0; i < S; ++i)
-      if (i < total && i >= p.prewait) issue(i);
-    prefetch_ahead(S);
+      if (i < total) issue(i);
     build_bc<WARPS>(p, frag, small, nchunks_frag, br);
   } else {
     build_fragments<M, WARPS, BC>(p, frag, small, 0, MM, nchunks_frag, nullptr);
   }
   __syncthreads();
-  if (!p.early_trigger) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   const float gsc = FP8 ? 1.0f : __ldg(p.gscale);
   const unsigned int* rowmax = reinterpret_cast<const unsigned int*>(small + kSmallRowmax);
@@ -1036,47 +1016,52 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
     }
   };
 
-  // A unit's K range is done: combine the tile's partials (last warp to finish
-  // it, fixed order over the K parts) and emit the tile.
-  auto finish_unit = [&](int j) {
-    const int u = warp + WARPS * j, tl = u / ks, kp = u % ks;
-    const int64_t tile = (int64_t)tile0 + (int64_t)tstep * tl;
-    bool last = true;
+  // Emit a finished tile.  Block columns: rg, rh are the sums of rows g, g + 8
+  // (lanes t == 0 emit them); otherwise acc[cg][0..3] hold the lane's outputs.
+  auto emit_bc = [&](int64_t tile, float rg, float rh) {
+    const int64_t rows[2] = {tile * 16 + g, tile * 16 + g + 8};
+    const float vals[2] = {rg, rh};
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+      if (rows[h] < p.n)  // inv is a power of two: (v inv) g == v (inv g) exactly
+        emit(0, 0, rows[h], 0, vals[h] * inv[0][0], ((int)(tile & 1) << 4) + g + 8 * h);
+  };
+  auto emit_tile = [&](int64_t tile) {
+    const int64_t rows[2] = {tile * 16 + g, tile * 16 + g + 8};
+#pragma unroll
+    for (int cg = 0; cg < NCG; ++cg)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        if (rows[h] >= p.n) continue;
+#pragma unroll
+        for (int e = 0; e < NE; ++e) {
+          const int mm = 8 * cg + 2 * t + e;
+          if (mm >= MM) continue;
+          const float v = (acc[cg][2 * h + e] * inv[cg][e]) * (FP8 ? rsc[h] : gsc);
+          emit(cg, e, rows[h], mm, v, ((int)(tile & 1) << 4) + g + 8 * h);
+        }
+      }
+  };
+
+  // A unit's K range is done.  A whole tile (ks = 1) is emitted now; a K
+  // part's sums go to its slot, and the tile is combined once every warp has
+  // streamed its units (after the main loop).
+  auto finish_unit = [&](const UnitCursor& c) {
+    const int64_t tile = (int64_t)tile0 + c.tl;
     if constexpr (BC) {
       float rg = acc[0][0] + acc[0][1], rh = acc[0][2] + acc[0][3];
       rg += __shfl_xor_sync(0xFFFFFFFFu, rg, 1);
       rh += __shfl_xor_sync(0xFFFFFFFFu, rh, 1);
       rg += __shfl_xor_sync(0xFFFFFFFFu, rg, 2);
       rh += __shfl_xor_sync(0xFFFFFFFFu, rh, 2);
-      if (ks > 1) {
-        float* slot = part + (tl * ks) * 16;
-        if (t == 0) {
-          slot[kp * 16 + g] = rg;
-          slot[kp * 16 + g + 8] = rh;
+      if (t == 0) {
+        if (ks > 1) {
+          float* slot = part + (size_t)(c.tl * ks + c.kp) * 16;
+          slot[g] = rg;
+          slot[g + 8] = rh;
+        } else {
+          emit_bc(tile, rg, rh);
         }
-        __syncwarp();
-        unsigned int prev = 0;
-        if (lane == 0) {
-          __threadfence_block();
-          prev = atomicAdd(tcnt + tl, 1u);
-        }
-        last = __shfl_sync(0xFFFFFFFFu, prev, 0) == (unsigned)(ks - 1);
-        if (last) {
-          __threadfence_block();
-          rg = rh = 0.f;
-          for (int q = 0; q < ks; ++q) {
-            rg += slot[q * 16 + g];
-            rh += slot[q * 16 + g + 8];
-          }
-        }
-      }
-      if (last && t == 0) {
-        const int64_t rows[2] = {tile * 16 + g, tile * 16 + g + 8};
-        const float vals[2] = {rg, rh};
-#pragma unroll
-        for (int h = 0; h < 2; ++h)
-          if (rows[h] < p.n)  // inv is a power of two: (v inv) g == v (inv g) exactly
-            emit(0, 0, rows[h], 0, vals[h] * inv[0][0], ((int)(tile & 1) << 4) + g + 8 * h);
       }
     } else {
 #pragma unroll
@@ -1084,47 +1069,13 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
 #pragma unroll
         for (int i = 0; i < 4; ++i) acc[cg][i] += acc[cg][4 + i];
       if (ks > 1) {
-        float* slot = part + ((size_t)(tl * ks) * 32 + lane) * (4 * NCG);
-        float* mine = slot + (size_t)kp * 32 * 4 * NCG;
+        float* mine = part + ((size_t)(c.tl * ks + c.kp) * 32 + lane) * (4 * NCG);
 #pragma unroll
         for (int cg = 0; cg < NCG; ++cg)
 #pragma unroll
           for (int i = 0; i < 4; ++i) mine[4 * cg + i] = acc[cg][i];
-        __syncwarp();
-        unsigned int prev = 0;
-        if (lane == 0) {
-          __threadfence_block();
-          prev = atomicAdd(tcnt + tl, 1u);
-        }
-        last = __shfl_sync(0xFFFFFFFFu, prev, 0) == (unsigned)(ks - 1);
-        if (last) {
-          __threadfence_block();
-#pragma unroll
-          for (int cg = 0; cg < NCG; ++cg) acc[cg][0] = acc[cg][1] = acc[cg][2] = acc[cg][3] = 0.f;
-          for (int q = 0; q < ks; ++q) {
-            const float* o = slot + (size_t)q * 32 * 4 * NCG;
-#pragma unroll
-            for (int cg = 0; cg < NCG; ++cg)
-#pragma unroll
-              for (int i = 0; i < 4; ++i) acc[cg][i] += o[4 * cg + i];
-          }
-        }
-      }
-      if (last) {
-        const int64_t rows[2] = {tile * 16 + g, tile * 16 + g + 8};
-#pragma unroll
-        for (int cg = 0; cg < NCG; ++cg)
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            if (rows[h] >= p.n) continue;
-#pragma unroll
-            for (int e = 0; e < NE; ++e) {
-              const int mm = 8 * cg + 2 * t + e;
-              if (mm >= MM) continue;
-              const float v = (acc[cg][2 * h + e] * inv[cg][e]) * (FP8 ? rsc[h] : gsc);
-              emit(cg, e, rows[h], mm, v, ((int)(tile & 1) << 4) + g + 8 * h);
-            }
-          }
+      } else {
+        emit_tile(tile);
       }
     }
 #pragma unroll
@@ -1136,11 +1087,11 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
   // ---- main loop over this warp's stages
   int cj = 0, ci = 0, c_ib = 0, c_len = 0;
   uint32_t so0 = 0, so1 = 0;  // without scale_tma: 16-bit scale-pair offsets of rows g, g+8 (n k / 32 < 2^31)
-  auto set_cunit = [&](int j) {
-    const int u = warp + WARPS * j, kp = u % ks;
-    c_ib = kp_begin(kp);
-    c_len = kp_begin(kp + 1) - c_ib;
-    const int tile = tile0 + tstep * (u / ks);
+  UnitCursor cc = first;
+  auto set_cunit = [&]() {
+    c_ib = kp_begin(cc.kp);
+    c_len = kp_begin(cc.kp + 1) - c_ib;
+    const int tile = tile0 + cc.tl;
     load_unit_extras(tile);
     if constexpr (!FP8) {
       int r0 = tile * 16 + g, r1 = r0 + 8;
@@ -1150,7 +1101,7 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
       so1 = (uint32_t)r1 * (uint32_t)(p.k / 32) + t;
     }
   };
-  if (nunits > 0) set_cunit(0);
+  if (nunits > 0) set_cunit();
   for (int q0 = 0; q0 < total; q0 += S) {
 #pragma unroll
     for (int i = 0; i < S; ++i) {
@@ -1198,9 +1149,10 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
         __syncwarp();  // every lane is done with stage i before it is refilled
         if (q + S < total) issue(i);
         if (++ci == c_len) {
-          finish_unit(cj);
+          finish_unit(cc);
           ci = 0;
-          if (++cj < nunits) set_cunit(cj);
+          cc.next(ks);
+          if (++cj < nunits) set_cunit();
         }
       }
     }
@@ -1214,6 +1166,40 @@ gemv_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ 
     for (int q = failed_at; q < total && q < failed_at + S; ++q)
       mbar_wait(bars + 8 * (q % S), (uint32_t)(q / S) & 1u, p.dev_status);
     if (threadIdx.x == 0 && prepped) mbar_wait(fbar, 0u, p.dev_status);  // thread 0's fragment copy
+  }
+
+  // Tiles split over K parts: once every warp has streamed its units, each
+  // tile's part sums are added in K-part order (the same for every tile, so
+  // equal weight rows give equal logits) and the tile is emitted.
+  if (ks > 1) {
+    __syncthreads();
+    for (int tl = warp; tl < nt; tl += WARPS) {
+      const int64_t tile = (int64_t)tile0 + tl;
+      load_unit_extras((int)tile);
+      if constexpr (BC) {
+        if (t == 0) {
+          const float* slot = part + (size_t)tl * ks * 16;
+          float rg = 0.f, rh = 0.f;
+          for (int q = 0; q < ks; ++q) {
+            rg += slot[q * 16 + g];
+            rh += slot[q * 16 + g + 8];
+          }
+          emit_bc(tile, rg, rh);
+        }
+      } else {
+        const float* slot = part + ((size_t)tl * ks * 32 + lane) * (4 * NCG);
+#pragma unroll
+        for (int cg = 0; cg < NCG; ++cg) acc[cg][0] = acc[cg][1] = acc[cg][2] = acc[cg][3] = 0.f;
+        for (int q = 0; q < ks; ++q) {
+          const float* o = slot + (size_t)q * 32 * 4 * NCG;
+#pragma unroll
+          for (int cg = 0; cg < NCG; ++cg)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) acc[cg][i] += o[4 * cg + i];
+        }
+        emit_tile(tile);
+      }
+    }
   }
 
   if (p.keys == nullptr) return;
@@ -1378,12 +1364,12 @@ KernelFn kernel_for12(int m) {
 }
 
 struct Layout {
-  uint32_t off_frag, off_zero, off_part, off_tcnt, off_small, off_kred, off_bar;
+  uint32_t off_frag, off_zero, off_part, off_small, off_kred, off_bar;
   size_t bytes;  // dynamic shared memory to request (includes 1 KB alignment slack)
 };
 
 // Shared-memory carve-up: ring | activations (+ zero area) | split-K partials |
-// tile counters | prologue scratch | argmax reduction | ring barriers.
+// prologue scratch | argmax reduction | ring barriers.
 Layout layout_for(int warps, int m, int nchunks, bool fp8, bool bc, int part_slots, bool argmax) {
   const int S = ring_depth(fp8);
   const int cols = m <= 8 ? m : 16, ncg = (m + 7) / 8;  // the kernel's M, column groups
@@ -1396,8 +1382,6 @@ Layout layout_for(int warps, int m, int nchunks, bool fp8, bool bc, int part_slo
   off += bc ? (size_t)warps * 8 * sizeof(BcRun) : 0;
   l.off_part = (uint32_t)off;
   off += (size_t)part_slots * (bc ? 16 : 32 * 4 * ncg) * sizeof(float);
-  l.off_tcnt = (uint32_t)off;
-  off += kMaxKs * sizeof(unsigned int);
   off = (off + 15) & ~(size_t)15;
   l.off_small = (uint32_t)off;
   off += (size_t)small_floats(warps) * sizeof(float);
@@ -1440,17 +1424,22 @@ int launch_rows(const GemvParams& base, const WeightRef& w, cudaStream_t stream,
     if (bc && wv != 16) break;
     const int mk = m <= 8 ? m : 16;  // the kernel's M
     if (wv == 12 && mk != 8 && mk != 16) continue;
-    const int ks = std::max(1, std::min({wv / p.tpc, p.nitems, kMaxKs}));
-    const Layout l = layout_for(wv, m, nchunks, w.fp8, bc, ks > 1 ? p.tpc * ks : 0, p.keys != nullptr);
     KernelFn f = bc ? bc_kernel()
                : wv == 16 ? (w.fp8 ? kernel_for<16, true>(m) : kernel_for<16, false>(m))
                : wv == 12 ? (w.fp8 ? kernel_for12<true>(mk) : kernel_for12<false>(mk))
                           : (w.fp8 ? kernel_for<8, true>(m) : kernel_for<8, false>(m));
+    // split K only where a CTA has at most half as many tiles as warps: with
+    // more, every warp already streams whole tiles, and splitting them so that
+    // the last idle warps join in measured slower (14 tiles of 4096 on 16
+    // warps: 18.9 us split 8 ways against 17.9 us whole)
+    const int ks = std::max(1, std::min({wv / p.tpc, p.nitems, kMaxKs}));
+    const Layout l = layout_for(wv, m, nchunks, w.fp8, bc, ks > 1 ? p.tpc * ks : 0, p.keys != nullptr);
     if (nvfp4::occupancy(reinterpret_cast<const void*>(f), wv * 32, l.bytes) >= 1) {
       fn = f;
       lay = l;
       warps = wv;
       p.ks = ks;
+      for (int i = 0; i <= ks; ++i) p.kbeg[i] = (int)((int64_t)i * p.nitems / ks);
       break;
     }
   }
@@ -1471,14 +1460,9 @@ int launch_rows(const GemvParams& base, const WeightRef& w, cudaStream_t stream,
   p.off_frag = lay.off_frag;
   p.off_zero = lay.off_zero;
   p.off_part = lay.off_part;
-  p.off_tcnt = lay.off_tcnt;
   p.off_small = lay.off_small;
   p.off_kred = lay.off_kred;
   p.off_bar = lay.off_bar;
-  p.early_trigger = 0;
-  p.interleave = 0;
-  p.prewait = 0;
-  p.l2_ahead = 0;
 
   CUtensorMap tmap;
   const int64_t row_bytes = w.fp8 ? w.k : w.k / 2;

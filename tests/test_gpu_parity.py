@@ -253,6 +253,14 @@ def test_gemv_rmsnorm_fused(dev):
     run_gemv_case(workloads.lm_head_m1(n=3000, k=1024, rows=4), dev)
 
 
+@pytest.mark.parametrize("n,k", [(24437, 2048), (16 * 152 * 9 + 3, 1024)])
+def test_gemv_m1_split_k_over_many_tiles(dev, n, k):
+    """M = 1 with 10 and 11 tiles per CTA on 152 SMs: whole tiles as contiguous
+    runs over 16 warps with the idle warps between busy ones; ragged last tile
+    and a last CTA with fewer tiles."""
+    run_gemv_case(workloads.lm_head_m1(n=n, k=k, rows=1), dev)
+
+
 def test_gemv_two_segment_concat_bf16_out(dev):
     run_gemv_case(workloads.fc_combiner(n=640, k_seg=512, m=5), dev, with_bf16=True)
 
