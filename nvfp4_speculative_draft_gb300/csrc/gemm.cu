@@ -212,6 +212,34 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// Transpose of 16-byte pieces within each group of G lanes (G = 4 or 8): on
+// entry lane gG + a holds pieces b = 0..G-1 (8 consecutive BF16 each) of its
+// own row a; on exit lane gG + b holds piece b of rows a = 0..G-1 in slot a.
+// Rounds m = 1, 2 (, 4) swap, between lanes l and l ^ m, the pieces whose
+// (lane ^ slot) bit m is set.
+template <int G>
+__device__ __forceinline__ void transpose_pieces(uint4 (&P)[G], int lane) {
+#pragma unroll
+  for (int m = 1; m < G; m <<= 1) {
+    const bool hi = (lane & m) != 0;
+#pragma unroll
+    for (int s0 = 0; s0 < G; ++s0) {
+      if (s0 & m) continue;
+      const int s1 = s0 | m;
+      const uint4 snd = hi ? P[s0] : P[s1];
+      uint4 rcv;
+      rcv.x = __shfl_xor_sync(0xFFFFFFFFu, snd.x, m);
+      rcv.y = __shfl_xor_sync(0xFFFFFFFFu, snd.y, m);
+      rcv.z = __shfl_xor_sync(0xFFFFFFFFu, snd.z, m);
+      rcv.w = __shfl_xor_sync(0xFFFFFFFFu, snd.w, m);
+      if (hi)
+        P[s0] = rcv;
+      else
+        P[s1] = rcv;
+    }
+  }
+}
+
 __device__ __forceinline__ uint4 ld_nc_u4(const void* p) {
   uint4 v;
   asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
@@ -512,47 +540,94 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_con
       tc_fence_after();
       int64_t m0, n0;
       tile_coords<BN>(p, (int)blockIdx.x + it * (int)gridDim.x, m0, n0);
-      constexpr int kChunks = (BN + 31) / 32;  // 32-column TMEM loads, a last 16 when BN % 32 == 16
+      // Each half's rows in 64-column pieces (two 32-column TMEM loads, an 8 x 8
+      // transpose of 16-byte pieces within each group of 8 lanes, then 8 stores
+      // that each write 4 rows x 128 contiguous bytes), and at BN = 240 the last
+      // 48 columns as 32 + 16 (4-lane groups: 8 rows x 64 bytes per store).
+      // Columns are stored up to n; rows up to m.
+      constexpr int kWide = BN / 64, kRest = BN - 64 * kWide;
+      const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16);
 #pragma unroll 1
-      for (int hj = 0; hj < kMHalves * kChunks; ++hj) {
-        const int h = hj / kChunks, col = 32 * (hj % kChunks);
-        const int w = BN - col >= 32 ? 32 : 16;
-        const int64_t row = m0 + h * BM + 32 * q + lane;
+      for (int h = 0; h < kMHalves; ++h) {
+        const int64_t rbase = m0 + h * BM + 32 * q;  // the warp's first row
+        const int64_t row = rbase + lane;
         const float rs = (F16 && row < p.m) ? __ldg(p.row_inv + row) : 1.0f;
-        const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)((ab * kMHalves + h) * kAccStride + col);
-        uint32_t v[32];
-        if (w == 32) {
-          tmem_ld32(taddr, v);
-        } else {
-          uint32_t v16[16];
-          tmem_ld16(taddr, v16);
+        const uint32_t tacc = tq + (uint32_t)((ab * kMHalves + h) * kAccStride);
+        const bool last_half = h == kMHalves - 1;
+        auto convert = [&](const uint32_t (&v)[32], uint4* P, int npieces) {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) v[i] = v16[i];
+          for (int i = 0; i < 4; ++i) {
+            if (i >= npieces) {
+              P[i] = make_uint4(0u, 0u, 0u, 0u);
+              continue;
+            }
+            uint32_t w4[4];
 #pragma unroll
-          for (int i = 16; i < 32; ++i) v[i] = 0u;
-        }
-        // columns stored: up to n (a multiple of 16 from the tile start)
-        const int64_t nvalid = p.n - (n0 + col);
-        const int ws = nvalid >= w ? w : (nvalid > 0 ? (int)nvalid : 0);
-        if (row < p.m && ws > 0) {
-          uint32_t packed16[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            __nv_bfloat162 b2 = __floats2bfloat162_rn((__uint_as_float(v[2 * i]) * rs) * gs,
-                                                      (__uint_as_float(v[2 * i + 1]) * rs) * gs);
-            packed16[i] = *reinterpret_cast<uint32_t*>(&b2);
+            for (int e = 0; e < 4; ++e) {
+              __nv_bfloat162 b2 = __floats2bfloat162_rn((__uint_as_float(v[8 * i + 2 * e]) * rs) * gs,
+                                                        (__uint_as_float(v[8 * i + 2 * e + 1]) * rs) * gs);
+              w4[e] = *reinterpret_cast<uint32_t*>(&b2);
+            }
+            P[i] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
           }
-          uint4* dst = reinterpret_cast<uint4*>(p.c + row * p.ldc + n0 + col);
+        };
+        auto release_if_done = [&](bool done) {  // TMEM fully read: the next tile may start
+          if (done) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tmem_empty(ab));
+          }
+        };
+#pragma unroll 1
+        for (int c = 0; c < kWide; ++c) {
+          uint4 P[8];
+          uint32_t v[32];
+          tmem_ld32(tacc + (uint32_t)(64 * c), v);
+          convert(v, P, 4);
+          tmem_ld32(tacc + (uint32_t)(64 * c + 32), v);
+          release_if_done(last_half && kRest == 0 && c == kWide - 1);
+          convert(v, P + 4, 4);
+          transpose_pieces<8>(P, lane);
+          const int j = lane & 7;
+          const int64_t cc = n0 + 64 * c + 8 * j;
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            if (8 * i < ws)
-              dst[i] = make_uint4(packed16[4 * i], packed16[4 * i + 1], packed16[4 * i + 2],
-                                  packed16[4 * i + 3]);
+          for (int k = 0; k < 8; ++k) {
+            const int64_t r = rbase + (lane & ~7) + k;
+            if (r < p.m && cc < p.n) *reinterpret_cast<uint4*>(p.c + r * p.ldc + cc) = P[k];
+          }
+        }
+        if constexpr (kRest > 0) {
+          static_assert(kRest == 48, "the last columns are one 32-column and one 16-column load");
+#pragma unroll 1
+          for (int u = 0; u < 2; ++u) {
+            const int col = 64 * kWide + 32 * u;
+            uint4 P[4];
+            uint32_t v[32];
+            if (u == 0) {
+              tmem_ld32(tacc + (uint32_t)col, v);
+            } else {
+              uint32_t v16[16];
+              tmem_ld16(tacc + (uint32_t)col, v16);
+#pragma unroll
+              for (int i = 0; i < 16; ++i) v[i] = v16[i];
+#pragma unroll
+              for (int i = 16; i < 32; ++i) v[i] = 0u;
+            }
+            release_if_done(last_half && u == 1);
+            convert(v, P, u == 0 ? 4 : 2);
+            transpose_pieces<4>(P, lane);
+            const int j = lane & 3;
+            const int64_t cc = n0 + col + 8 * j;
+            if (u == 0 || j < 2) {
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const int64_t r = rbase + (lane & ~3) + k;
+                if (r < p.m && cc < p.n) *reinterpret_cast<uint4*>(p.c + r * p.ldc + cc) = P[k];
+              }
+            }
+          }
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(tmem_empty(ab));
     }
   }
   tc_fence_before();
