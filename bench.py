@@ -345,24 +345,21 @@ def time_graph(fn, stream, iters, warmup=3):
 
 
 def time_flushed(fn, stream, iters, warmup=3):
-    """Time fn alone, `iters` times, each after writing a 256 MB buffer (twice
-    the L2) on the same stream so that no call finds the previous call's data
-    in L2; returns the mean of the per-call event times."""
+    """Time fn with a cold L2.  One CUDA graph writes a 256 MB buffer (twice the
+    L2) and then runs fn; a second graph only writes the buffer.  Both are
+    replayed `iters` times (events on the stream, no host launch gaps inside a
+    replay), and fn's time is the difference of the per-replay times, so it
+    includes the write-back of fn's outputs that the next buffer write forces."""
     assert torch.cuda.current_stream() == stream
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=stream.device)
-    for _ in range(warmup):
+
+    def flush_then_fn():
         flush.fill_(1)
         fn()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(iters)]
-    torch.cuda.synchronize()
-    for a, b in ev:
-        flush.fill_(1)
-        a.record(stream)
-        fn()
-        b.record(stream)
-    torch.cuda.synchronize()
-    return sum(a.elapsed_time(b) for a, b in ev) / iters
+
+    t_both = time_graph(flush_then_fn, stream, iters, warmup)
+    t_flush = time_graph(lambda: flush.fill_(1), stream, iters, warmup)
+    return t_both - t_flush
 
 
 def bench_details(dev, stream, hbm, bf16):
@@ -448,7 +445,8 @@ def bench_details(dev, stream, hbm, bf16):
     fp8["quantize"] = {"us": msq * 1e3, "GBps": qb8 / msq / 1e6,
                        "frac_of_measured_hbm": qb8 / msq / 1e6 / hbm,
                        "note": "BF16 read once (each row's second pass hits L2) + codes + row "
-                               "scales; L2 flushed before each timed call"}
+                               "scales; L2 flushed before each call (graph of flush + call, "
+                               "minus a graph of the flush alone)"}
     out["fp8w_propose_151936x5120"] = fp8
     del w8, case_w
     out["chained_propose_step"] = {"us_per_step": ms * 1e3, "GBps": b / ms / 1e6,
@@ -507,7 +505,8 @@ def bench_details(dev, stream, hbm, bf16):
                                   "note": "bytes = two passes over the BF16 weight (absmax, "
                                           "quantise) + codes + scales; the quantise pass runs "
                                           "backwards and finds the absmax pass's last reads in "
-                                          "L2; L2 flushed before each timed call"}
+                                          "L2; L2 flushed before each call (graph of flush + "
+                                          "call, minus a graph of the flush alone)"}
     return out
 
 
