@@ -1363,6 +1363,14 @@ KernelFn kernel_for12(int m) {
   }
 }
 
+// 13 warps: the 16-row kernel, whose 63-tile CTAs then give every warp at
+// most 5 tiles instead of 6 (the rings of 13 warps still fit beside 16 rows of
+// 5120 activations)
+template <bool FP8>
+KernelFn kernel_for13(int m) {
+  return m == 16 ? gemv_kernel<16, 13, FP8, false> : nullptr;
+}
+
 struct Layout {
   uint32_t off_frag, off_zero, off_part, off_small, off_kred, off_bar;
   size_t bytes;  // dynamic shared memory to request (includes 1 KB alignment slack)
@@ -1417,15 +1425,17 @@ int launch_rows(const GemvParams& base, const WeightRef& w, cudaStream_t stream,
   Layout lay{};
   int warps = 0;
   // 16 warps of up to 128 registers (one CTA per SM; 32 warps at 64
-  // registers and 2 CTAs of 16 warps both measured slower), or 12 (8 and 16
-  // rows) or 8 warps when the activations leave too little shared memory for
-  // 16 rings
-  for (int wv : {16, 12, 8}) {
+  // registers and 2 CTAs of 16 warps both measured slower), or 13 (16 rows),
+  // 12 (8 and 16 rows) or 8 warps when the activations leave too little
+  // shared memory for 16 rings
+  for (int wv : {16, 13, 12, 8}) {
     if (bc && wv != 16) break;
     const int mk = m <= 8 ? m : 16;  // the kernel's M
     if (wv == 12 && mk != 8 && mk != 16) continue;
+    if (wv == 13 && mk != 16) continue;
     KernelFn f = bc ? bc_kernel()
                : wv == 16 ? (w.fp8 ? kernel_for<16, true>(m) : kernel_for<16, false>(m))
+               : wv == 13 ? (w.fp8 ? kernel_for13<true>(mk) : kernel_for13<false>(mk))
                : wv == 12 ? (w.fp8 ? kernel_for12<true>(mk) : kernel_for12<false>(mk))
                           : (w.fp8 ? kernel_for<8, true>(m) : kernel_for<8, false>(m));
     // split K only where a CTA has at most half as many tiles as warps: with
