@@ -23,8 +23,12 @@
 //                same 128-byte-swizzled K-major layout, fence the async proxy
 //                and arrive on the stage's "full" barrier;
 //   last 4 warps epilogue: tcgen05.ld of their TMEM lane quadrant for both
-//                halves, times g, round to BF16, store (up to n); then release
-//                TMEM to the next tile.
+//                halves, 32 columns at a time, times g, round to BF16; each
+//                64-column piece is transposed in 16-byte units across 8
+//                lanes (shuffles), so one store instruction writes 4 rows x
+//                128 contiguous bytes rather than 32 rows x 16 bytes; stores
+//                up to n and m; TMEM goes back to the next tile right after
+//                its last load.
 // Dequantisation: E2M1 nibble pairs become BF16 bit patterns of value * 2^-126
 // (integer ops), then one packed BF16 multiply by the block scale * 2^118
 // (exact); the 2^8 left over is folded into g in the epilogue.
