@@ -316,15 +316,18 @@ quantize_kernel(const uint4* __restrict__ w, int64_t nblocks, const uint32_t* __
     // before the grid-dependency wait
     if (lane != 0) return;
     int64_t it = 0;
+    int st = 0;          // stage of chunk it (it mod kQuantStages)
+    uint32_t ph = 0u;    // parity of its round (it / kQuantStages)
     for (int64_t c = blockIdx.x; c < nchunks; c += gridDim.x, ++it) {
-      const int st = (int)(it % kQuantStages);
-      if (it >= kQuantStages &&
-          !mbar_wait(empty0 + 8 * st, (uint32_t)((it / kQuantStages - 1) & 1), dev_status))
-        break;
+      if (it >= kQuantStages && !mbar_wait(empty0 + 8 * st, ph ^ 1u, dev_status)) break;
       const int64_t nb = nblocks - c * kChunkBlocks;
       const uint32_t bytes = (uint32_t)(nb < kChunkBlocks ? nb : kChunkBlocks) * 32u;
       mbar_arrive_expect_tx(full0 + 8 * st, bytes);
       bulk_copy_g2s(ring_base + st * kChunkBytes, w + c * (kChunkBlocks * 2), bytes, full0 + 8 * st);
+      if (++st == kQuantStages) {
+        st = 0;
+        ph ^= 1u;
+      }
     }
     // every issued copy has landed before this thread (and so the CTA) exits
     const int64_t first = it > kQuantStages ? it - kQuantStages : 0;
@@ -345,13 +348,14 @@ quantize_kernel(const uint4* __restrict__ w, int64_t nblocks, const uint32_t* __
   const float t6hi = fast6 ? __fmul_ru(__frcp_ru(six_g), 1.0f + 0x1p-22f) : 0.0f;
   asm volatile("bar.sync 1, %0;" ::"n"(kQuantWarps * 32) : "memory");  // compute warps only
   const bool scales_even = (reinterpret_cast<uintptr_t>(scales) & 1u) == 0;
-  int64_t it = 0;
-  for (int64_t c = blockIdx.x; c < nchunks; c += gridDim.x, ++it) {
-    const int st = (int)(it % kQuantStages);
-    if (!mbar_wait(full0 + 8 * st, (uint32_t)((it / kQuantStages) & 1), dev_status)) break;
-    // blocks 2t, 2t + 1 of the chunk: 64 contiguous bytes in, 16 bytes of
-    // codes and 2 scale bytes out
-    const int64_t b0 = c * kChunkBlocks + 2 * threadIdx.x;
+  int st = 0;        // stage of the current chunk (its index mod kQuantStages)
+  uint32_t ph = 0u;  // parity of its round
+  const int64_t bstep = (int64_t)gridDim.x * kChunkBlocks;
+  int64_t b0 = (int64_t)blockIdx.x * kChunkBlocks + 2 * threadIdx.x;
+  for (int64_t c = blockIdx.x; c < nchunks; c += gridDim.x, b0 += bstep) {
+    if (!mbar_wait(full0 + 8 * st, ph, dev_status)) break;
+    // blocks 2t, 2t + 1 of the chunk (b0, b0 + 1): 64 contiguous bytes in,
+    // 16 bytes of codes and 2 scale bytes out
     const int nb = b0 + 1 < nblocks ? 2 : (b0 < nblocks ? 1 : 0);
     uint4 v[4];
     const uint32_t src = ring_base + st * kChunkBytes + threadIdx.x * 64u;
@@ -377,6 +381,10 @@ quantize_kernel(const uint4* __restrict__ w, int64_t nblocks, const uint32_t* __
     } else if (nb == 1) {
       packed[b0] = q0.codes;
       scales[b0] = (uint8_t)q0.scale;
+    }
+    if (++st == kQuantStages) {
+      st = 0;
+      ph ^= 1u;
     }
   }
   // The GEMV reads its weights before its grid-dependency wait (they are
