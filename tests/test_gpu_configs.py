@@ -179,6 +179,25 @@ def test_propose_config_full_width(dev):
             assert abs(float(lp[r]) - own) <= 1e-5 * (1 + abs(float(lg[r, i])))
 
 
+def test_propose_16_rows_full_width(dev):
+    """The 151936 x 5120 head at 16 batch rows (the draft width the benchmark
+    times: two MMA column groups, 63 whole tiles per CTA shared by the warps):
+    every logit of every row against the oracle, and each row's argmax by the
+    top-2-gap rule."""
+    m = nd()
+    case = workloads.propose_m8(m=16, device=dev)
+    wq, _ = m.nvfp4_quantize(case.w)
+    del case.w
+    x = case.segments[0][0]
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    logits, idx = m.w4a16_gemv_argmax([(x, None)], wq, dev_status=status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    g = np.float32(wq.global_scale.item())
+    ys, ss = par_gemv(workloads.bits(x), wq.packed.cpu().numpy(), wq.scales.cpu().numpy(), g)
+    check_logits_and_argmax(logits.cpu().numpy(), idx.cpu().numpy(), ys, ss)
+
+
 @pytest.mark.parametrize("mm", [1, 4, 8])
 def test_fc_combiner_config_full(dev, mm):
     """5120 x 10240 fc over RMSNorm(e) ++ RMSNorm(h), BF16 output, every output."""
