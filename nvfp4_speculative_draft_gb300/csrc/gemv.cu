@@ -10,8 +10,10 @@
 //     y[m, n]   = g * sum_i a[m, i] * e4m3(s[n, i/16]) * e2m1(c[n, i])      (FP32)
 //     argmax[m] = lowest n with y[m, n] maximal (NaN never wins)
 //
-// Design.  The kernel is bound by streaming the weights from HBM (NVFP4: 0.5625
-// byte per weight incl. scales; FP8: 1 byte + 4 per row).
+// Design.  The kernel streams the weights from HBM once (NVFP4: 0.5625 byte
+// per weight incl. scales; FP8: 1 byte + 4 per row); with NVFP4 weights the
+// decode and the legacy MMAs keep the SM's issue slots about half busy, so the
+// main loop runs somewhat below the copy rate.
 //   * Work split: one CTA per SM (grid <= SM count), each owning a contiguous,
 //     equal range of 16-row tiles, so every SM streams the same number of weight
 //     bytes.  Inside the CTA each warp takes a contiguous run of the CTA's
@@ -24,13 +26,16 @@
 //     issues the TMA copy (cp.async.bulk.tensor) of a stage -- 256 K elements
 //     of 16 rows: one box of 16 rows x 128 bytes (NVFP4) or 16 x 256 bytes
 //     (FP8) -- with an mbarrier completion.  Rows past n and bytes past k
-//     arrive as zeros (TMA bounds fill).  NVFP4 block scales are prefetched
-//     into registers when a stage is issued.  (Two 64-byte-wide boxes per
-//     stage avoid a 2-way bank conflict on the code loads but measured slower:
-//     the TMA request count matters more.)
+//     arrive as zeros (TMA bounds fill).  NVFP4 block scales arrive in the
+//     same stage by a second TMA box (16 rows x 16 bytes) when k is a multiple
+//     of 256, else are read from global memory as the stage is computed.  (Two
+//     64-byte-wide boxes per stage avoid a 2-way bank conflict on the code
+//     loads but measured slower: the TMA request count matters more.)
 //   * Across calls: the weights, their scales and the norm weights are
-//     load-time constants, so a CTA issues its first ring stages (and reads the
-//     norm weights) before the grid-dependency wait.  Activations are read
+//     load-time constants, so with two or more rows a CTA issues its first
+//     ring stages (and reads the norm weights) before the grid-dependency
+//     wait; at M = 1 it issues them right after its activation loads, so that
+//     those are not queued behind the ring fills.  Activations are read
 //     only after the wait: normalised by every CTA for one row, or, with a
 //     large enough workspace and two or more rows, once per call by a small
 //     grid (one CTA per row) whose result every GEMV CTA copies.
